@@ -1,0 +1,438 @@
+"""Benchmark of the sm_103a pipelined tiled fp16 GEMM.
+
+One step = one GEMM C = A @ B (fp16 in, fp32 accumulate) over one batch of
+synthetic input.  The default workload is the compute-bound 8192^3 fp16-out
+product; ``--workload`` picks another of the five shapes.
+
+Prints ONE JSON line (rank 0):
+  value      TFLOP/s = 2MNK x ranks / (max over ranks of the timed seconds / steps),
+             inputs resident in HBM, rotated over 3 copies (each > L2)
+  e2e        the same metric through the public API with host buffers: the
+             H2D copy of A and B from pinned memory and the D2H copy of C are
+             inside the timed region
+  roofline   the GEMM kernel's achieved TFLOP/s (algorithmic flops / average
+             launch time from CUDA events) against the measured dense peak
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
+  clocks     SM clocks and throttle reasons sampled during the timed region
+
+``--impl reference`` times the CPU oracle instead (the reference arm): each
+step computes a bounded sample of rows of the same product on the host cores.
+
+Multi-GPU (torchrun, one rank per GPU): replicas only -- every rank runs the
+same full GEMM on its own GPU; there is no data-path collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s (fp16 in, fp32 acc) at 8192³; % of GB300 dense FP16 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["tensor_core_tiled_02_gb300/csrc/gemm_kernel.cuh", "tensor_core_tiled_02_gb300/csrc/ptx.cuh",
+                  "tensor_core_tiled_02_gb300/csrc/gemm_f16.cu"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gemm_8192")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---- distributed plumbing (replicas only) -------------------------------------
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend: str):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float, device=None) -> float:
+        if self.pg is None:
+            return x
+        import torch
+
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def aggregate(per_rank_seconds: list[float], flops_per_step: float, steps: int) -> dict:
+    """Whole-job throughput from every rank's timed seconds: all ranks' work
+    over the slowest rank's time (replicas: each rank ran `steps` GEMMs)."""
+    t = max(per_rank_seconds)
+    n = len(per_rank_seconds)
+    return {"seconds": t, "ms_per_step": 1e3 * t / steps, "tflops": n * flops_per_step * steps / t / 1e12}
+
+
+# ---- peaks, clocks, profiles -------------------------------------------------------
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+        self.enabled = enabled
+
+    def start(self):
+        if not self.enabled:
+            return
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows) -> dict | None:
+    def num(s):
+        try:
+            return float(s)
+        except ValueError:
+            return None
+
+    if not rows:
+        return None
+    sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+    mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+    pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = set()
+    for r in rows:
+        for name, v in zip(names, r[5:9]):
+            if v.strip().lower() in ("active", "1", "yes"):
+                reasons.add(name)
+    # samples under load: the upper part of the clock range (idle samples at the
+    # edges of the window are dropped by taking the samples with power near max)
+    loaded = sm
+    if pw and len(pw) == len(sm):
+        pmax = max(pw)
+        loaded = [s for s, p in zip(sm, pw) if p >= 0.6 * pmax] or sm
+    return {"sm_mhz": statistics.median(loaded) if loaded else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "power_w_max": max(pw) if pw else None,
+            "samples": len(rows),
+            "reasons": sorted(reasons)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, plan: dict) -> int | None:
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"gemm_f16_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m_hash and m_traffic) or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_traffic.group(1))
+
+
+# ---- the CPU oracle (baseline and reference arm) -----------------------------------
+
+
+def cpu_oracle_sample(a, b, w, budget_s: float, rows_per_call: int | None = None):
+    """Time the oracle on whole rows of the product; return (value TFLOP/s,
+    rows, seconds, threads).  B is decoded once before timing (inputs
+    resident), then rows are computed until about `budget_s` has passed."""
+    import numpy as np
+
+    import oracle
+
+    threads = os.cpu_count() or 1
+    dec = oracle.DecodedB(b.numpy())
+    a_np = a.numpy()
+    rng = np.random.default_rng(0)
+    per_call = rows_per_call or threads
+    # calibration call (also faults in pages), not counted
+    dec.gemm_rows(a_np, rng.integers(0, w.M, per_call), w.out_dtype, nthreads=threads)
+    done_rows = 0
+    t0 = time.perf_counter()
+    while True:
+        rows = rng.integers(0, w.M, per_call)
+        dec.gemm_rows(a_np, rows, w.out_dtype, nthreads=threads)
+        done_rows += per_call
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    flops = 2.0 * done_rows * w.N * w.K
+    return flops / el / 1e12, done_rows, el, threads
+
+
+def run_reference(args, w, dist: Dist):
+    """The reference arm: the CPU oracle, each step a bounded sample of rows."""
+    import numpy as np
+
+    import oracle
+    from tensor_core_tiled_02_gb300.synthetic import workload_inputs
+
+    if dist.rank != 0:
+        return 0
+    threads = os.cpu_count() or 1
+    a, b = workload_inputs(w)
+    dec = oracle.DecodedB(b.numpy())
+    a_np = a.numpy()
+    rng = np.random.default_rng(0)
+    rows_per_step = threads  # one whole row per thread per step
+    for _ in range(args.warmup):
+        dec.gemm_rows(a_np, rng.integers(0, w.M, rows_per_step), w.out_dtype, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        dec.gemm_rows(a_np, rng.integers(0, w.M, rows_per_step), w.out_dtype, nthreads=threads)
+    el = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
+    value = flops / el / 1e12
+    sample = (f"{rows_per_step} whole rows of the {w.M}x{w.N}x{w.K} product per step "
+              f"({rows_per_step}*{w.N} of {w.M * w.N} outputs), B decoded to fp64 once before timing")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": workload_config(w, None),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, plan) -> dict:
+    cfg = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+           "out_dtype": "f16" if w.out_dtype == 0 else "f32",
+           "inputs": f"A ~ {w.a_dist[0]}({w.a_dist[1]:g}), B ~ {w.b_dist[0]}({w.b_dist[1]:g}), fp16, seeds 0/1",
+           "l2": "inputs rotated over 3 copies, each larger than L2 (A+B+C > 126 MB)"}
+    if plan is not None:
+        cfg["plan"] = {k: plan[k] for k in ("tile_m", "tile_n", "tile_k", "stages", "release", "grid",
+                                            "raster_group", "num_tiles", "k_steps")}
+    return cfg
+
+
+# ---- our arm -----------------------------------------------------------------------
+
+
+def run_ours(args, w, dist: Dist):
+    import torch
+
+    import tensor_core_tiled_02_gb300 as tc
+    from tensor_core_tiled_02_gb300.synthetic import workload_inputs
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    out_t = torch.float16 if w.out_dtype == 0 else torch.float32
+    a_cpu, b_cpu = workload_inputs(w)
+    n_copies = 3
+    As = [a_cpu.to(dev) for _ in range(n_copies)]
+    Bs = [b_cpu.to(dev) for _ in range(n_copies)]
+    Cs = [torch.empty((w.M, w.N), dtype=out_t, device=dev) for _ in range(n_copies)]
+    plan = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype)
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+
+    def step(i):
+        j = i % n_copies
+        rc = tc.gemm_f16(As[j].data_ptr(), Bs[j].data_ptr(), Cs[j].data_ptr(), w.M, w.N, w.K, w.out_dtype, handle)
+        if rc != 0:
+            raise tc.GemmError(rc)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    rc, site = tc.gemm_f16_device_status(reset=True)
+    if rc != 0:
+        raise RuntimeError(f"device wait gave up during warm-up (site {site})")
+
+    # timed region: one launch per step, a CUDA event pair around each launch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dist.local_rank, enabled=not args.no_clocks)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step(i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clock_summary = clocks.stop()
+    seconds = start.elapsed_time(end) / 1e3
+    launch_ms = [s.elapsed_time(e) for s, e in ev]
+    avg_launch_s = statistics.fmean(launch_ms) / 1e3
+    rc, site = tc.gemm_f16_device_status(reset=True)
+    if rc != 0:
+        raise RuntimeError(f"device wait gave up in the timed region (site {site})")
+
+    t_max = dist.max(seconds, device=dev)
+    flops = float(w.flops)
+    value = dist.world * flops * args.steps / t_max / 1e12
+
+    # end to end through the public API with host buffers
+    a_h = a_cpu.pin_memory()
+    b_h = b_cpu.pin_memory()
+    c_h = torch.empty((w.M, w.N), dtype=out_t).pin_memory()
+    a_d, b_d, c_d = As[0], Bs[0], Cs[0]
+
+    def e2e_step():
+        a_d.copy_(a_h, non_blocking=True)
+        b_d.copy_(b_h, non_blocking=True)
+        tc.matmul(a_d, b_d, out_dtype=out_t, out=c_d)
+        c_h.copy_(c_d, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_s = dist.max(e0.elapsed_time(e1) / 1e3, device=dev)
+    e2e_value = dist.world * flops * args.e2e_steps / e2e_s / 1e12
+    h2d = (a_h.numel() + b_h.numel()) * 2
+    d2h = c_h.numel() * c_h.element_size()
+
+    if dist.rank == 0:
+        peaks, peak_src = load_peaks()
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        achieved = flops / avg_launch_s / 1e12
+        roofline = {
+            "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(w.name, plan),
+            "peak_source": f"bf16_tflops (burst) of {peak_src}; fp16 dense rate equals bf16 on this part",
+            "frac_of_sustained": achieved / peak_sus,
+            "kernel": f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>",
+            "avg_launch_ms": avg_launch_s * 1e3,
+        }
+        cpu = None
+        if not args.no_cpu_baseline and dist.world == 1:
+            v, rows, el, thr = cpu_oracle_sample(a_cpu, b_cpu, w, args.cpu_seconds)
+            cpu = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                   "sample": f"{rows} whole rows of the {w.M}x{w.N}x{w.K} product ({rows * w.N} of "
+                             f"{w.M * w.N} outputs) in {el:.1f} s, B decoded to fp64 once before timing"}
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": workload_config(w, plan),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": args.e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clock_summary,
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from tensor_core_tiled_02_gb300.synthetic import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    dist = Dist()
+    if args.impl == "reference":
+        return run_reference(args, w, dist)
+    return run_ours(args, w, dist)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

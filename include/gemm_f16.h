@@ -1,0 +1,152 @@
+/*
+ * gemm_f16.h - C ABI of the GB300 (sm_103a) pipelined tiled fp16 GEMM.
+ *
+ * The operation is the matmul of the "JAX Pallas Mosaic GPU quickstart",
+ * section "Hopper matrix multiplication kernel": matmul(a, b, out_dtype)
+ * with m, k = a.shape and _, n = b.shape, fp16 operands, an fp32 Tensor Core
+ * accumulator (plgpu.ACC) and a final conversion acc.astype(out_dtype):
+ *
+ *     C[i][j] = out_dtype( sum_k  A[i][k] * B[k][j] ),  accumulated in fp32.
+ *
+ * The parallel grid of output tiles, the sequential pipeline along K and its
+ * two knobs (max_concurrent_steps, delay_release) come from the same page's
+ * "Key emit_pipeline parameters" section and from the "Pallas software
+ * pipelining guide" (sections 3, 4 and 9.2).  Here they are realised with TMA,
+ * an mbarrier-guarded shared-memory ring, tcgen05.mma into Tensor Memory and
+ * a persistent tile scheduler.
+ *
+ * Conventions for every entry point:
+ *   - Matrices are dense and row-major: A is M x K (row stride K elements),
+ *     B is K x N (row stride N), C is M x N (row stride N).
+ *   - A, B and C are DEVICE pointers owned by the caller.  The library never
+ *     allocates, frees or synchronises them; it keeps only a small per-device
+ *     cache (SM count, kernel attributes) and one process-wide tuning config.
+ *   - Return value: 0 on success, a negative gemm_status code otherwise.
+ *     Argument checks run on the host before any CUDA call; no exceptions are
+ *     thrown and nothing is printed.
+ */
+#ifndef TCGEMM_GEMM_F16_H
+#define TCGEMM_GEMM_F16_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* One IEEE 754 binary16 value as stored in memory (same layout as CUDA's
+ * __half; pass a __half* with a cast). */
+typedef unsigned short gemm_f16_t;
+
+/* The same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *gemm_stream_t;
+
+typedef enum {
+    GEMM_OUT_F16 = 0, /* C is fp16, rounded to nearest even from the fp32 accumulator */
+    GEMM_OUT_F32 = 1  /* C is the fp32 accumulator */
+} gemm_out_dtype;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_NULL = -1,           /* a required pointer is NULL */
+    GEMM_ERR_DIM = -2,            /* M, N or K negative, or the problem too large to index */
+    GEMM_ERR_DTYPE = -3,          /* out_dtype not a gemm_out_dtype */
+    GEMM_ERR_ALIGN = -4,          /* a pointer not 16-byte aligned, or N or K not a multiple of 8
+                                     (TMA needs 16-byte-aligned rows) */
+    GEMM_ERR_ALIAS = -5,          /* C overlaps A or B (inputs are read-only, the output write-only) */
+    GEMM_ERR_CONFIG = -6,         /* invalid tuning config, e.g. release >= stages */
+    GEMM_ERR_TMAP = -7,           /* the driver refused a tensor-map encoding */
+    GEMM_ERR_LAUNCH = -8,         /* the kernel launch failed */
+    GEMM_ERR_CUDA = -9,           /* no usable CUDA device or driver entry point */
+    GEMM_ERR_ARCH = -10,          /* the current device is not compute capability 10.3 */
+    GEMM_ERR_DEVICE_TIMEOUT = -11 /* a kernel's bounded wait ran out (see gemm_f16_device_status) */
+} gemm_status;
+
+/* What the planner chose for one problem (gemm_f16_plan). */
+typedef struct {
+    int tile_m, tile_n, tile_k; /* output tile and K step (elements) */
+    int tiles_m, tiles_n;       /* ceil(M/tile_m), ceil(N/tile_n) */
+    int num_tiles;              /* tiles_m * tiles_n: one owner CTA each */
+    int k_steps;                /* ceil(K/tile_k): the sequential pipeline length */
+    int stages;                 /* shared-memory ring depth (max_concurrent_steps) */
+    int release;                /* extra buffer-release depth (delay_release) */
+    int grid;                   /* persistent CTAs launched */
+    int raster_group;           /* m-blocks per raster group */
+    int smem_bytes;             /* dynamic shared memory per CTA */
+    int tmem_cols;              /* Tensor Memory columns per CTA */
+    int threads;                /* threads per CTA */
+} gemm_plan;
+
+/* Tuning override.  Zero in a field means "planner default". */
+typedef struct {
+    int tile_n;            /* 0, 128 or 256 */
+    int stages;            /* 0 or 1..8 */
+    int release;           /* 0..7, must be < the stages used */
+    int grid;              /* 0 = min(num_tiles, SM count); else a cap on the CTAs launched */
+    int raster_group;      /* 0 or >= 1 */
+    long long wait_limit;  /* 0 = about one second; else clock cycles one device wait may take */
+    int inject_stall;      /* test hook: 1 makes every CTA's producer issue no loads, so
+                              the MMA warp's bounded wait runs out and the kernel reports
+                              GEMM_ERR_DEVICE_TIMEOUT instead of finishing.  0 in normal use. */
+} gemm_config;
+
+/*
+ * C = A * B (fp16 x fp16, fp32 accumulation), written as out_dtype.
+ *
+ *   A          device, M x K fp16, row-major, 16-byte aligned, read-only
+ *   B          device, K x N fp16, row-major, 16-byte aligned, read-only
+ *   C          device, M x N of out_dtype, row-major, 16-byte aligned; must not
+ *              overlap A or B; every element is written
+ *   M, N, K    >= 0; N and K multiples of 8 (16-byte rows for TMA).  M, N and K
+ *              need not be multiples of the tile: edge tiles are zero-filled on
+ *              load and clipped on store.  M == 0 or N == 0 is a no-op; K == 0
+ *              writes zeros (the empty sum).
+ *   out_dtype  GEMM_OUT_F16 or GEMM_OUT_F32
+ *   stream     CUDA stream the kernel is enqueued on; the call is asynchronous
+ *              and C is valid once the stream reaches this point
+ *
+ * Pointers may be NULL only where nothing is read or written through them
+ * (A and B when K == 0; all three when M == 0 or N == 0).
+ * Errors: GEMM_ERR_DTYPE, GEMM_ERR_DIM, GEMM_ERR_NULL, GEMM_ERR_ALIGN,
+ * GEMM_ERR_ALIAS, GEMM_ERR_CONFIG before any CUDA call; GEMM_ERR_CUDA,
+ * GEMM_ERR_ARCH, GEMM_ERR_TMAP, GEMM_ERR_LAUNCH after.  A device-side timeout
+ * is not seen here (the launch is asynchronous): read gemm_f16_device_status.
+ */
+int gemm_f16(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, int K, int out_dtype,
+             gemm_stream_t stream);
+
+/*
+ * The plan gemm_f16 would use for this problem under the current config.
+ * num_sms > 0 plans for that many SMs without touching CUDA (host-only);
+ * num_sms == 0 asks the current device.  `out` is caller-owned host memory.
+ * Errors: as gemm_f16's argument checks (pointers excepted), GEMM_ERR_NULL
+ * for out == NULL, GEMM_ERR_CUDA when num_sms == 0 and no device answers.
+ */
+int gemm_f16_plan(int M, int N, int K, int out_dtype, int num_sms, gemm_plan *out);
+
+/* Replace the process-wide tuning config (copied); NULL restores defaults.
+ * Not synchronised with concurrent gemm_f16 calls on other host threads.
+ * Errors: GEMM_ERR_CONFIG for an out-of-range field (the old config stays). */
+int gemm_f16_set_config(const gemm_config *cfg);
+
+/* Copy the current tuning config into caller-owned `out`. */
+int gemm_f16_get_config(gemm_config *out);
+
+/* Static, NUL-terminated description of a gemm_status code. */
+const char *gemm_f16_strerror(int code);
+
+/*
+ * Synchronise the current device, then report whether any kernel of this
+ * library gave up on a bounded wait since the last reset: GEMM_OK or
+ * GEMM_ERR_DEVICE_TIMEOUT.  *site (if not NULL) receives which wait gave up
+ * first (1 producer/empty slot, 2 MMA/full slot, 3 MMA/free accumulator,
+ * 4 epilogue/ready accumulator, 5 drain), 0 if none.  reset != 0 clears it.
+ */
+int gemm_f16_device_status(int *site, int reset);
+
+/* ABI version of this header: 1. */
+int gemm_f16_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCGEMM_GEMM_F16_H */

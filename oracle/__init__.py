@@ -64,6 +64,8 @@ def _bind(lib):
     lib.oracle_gemm_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
+    lib.oracle_gemm_rows_decoded.restype = ctypes.c_int
+    lib.oracle_gemm_rows_decoded.argtypes = lib.oracle_gemm_rows.argtypes
     lib.oracle_gemm.restype = ctypes.c_int
     lib.oracle_gemm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
@@ -151,6 +153,31 @@ def gemm(A, B, out_dtype: int = OUT_F16, rows=None, nthreads=None, lib=None) -> 
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_rows failed with {rc}")
     return out
+
+
+class DecodedB:
+    """B decoded once to fp64, for computing many row samples of one product."""
+
+    def __init__(self, B, lib=None):
+        self.lib = lib or load()
+        b = _u16(B)
+        self.K, self.N = b.shape
+        self.bd = np.empty(b.shape, np.float64)
+        self.lib.oracle_f16_decode_array(b.ctypes.data, self.bd.ctypes.data, b.size)
+
+    def gemm_rows(self, A, rows, out_dtype: int = OUT_F16, nthreads=None) -> np.ndarray:
+        a = _u16(A)
+        M, K = a.shape
+        if K != self.K:
+            raise ValueError("inner dimensions differ")
+        rows = np.ascontiguousarray(np.asarray(rows, np.int64)).ravel()
+        out = np.zeros((rows.size, self.N), _out_np_dtype(out_dtype))
+        rc = self.lib.oracle_gemm_rows_decoded(a.ctypes.data, self.bd.ctypes.data, out.ctypes.data, M,
+                                               self.N, K, out_dtype, rows.ctypes.data, rows.size,
+                                               _threads(nthreads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_gemm_rows_decoded failed with {rc}")
+        return out
 
 
 def gemm_elems(A, B, ii, jj, out_dtype: int = OUT_F16, lib=None) -> np.ndarray:

@@ -156,6 +156,9 @@ static void *row_worker(void *arg)
     return NULL;
 }
 
+int oracle_gemm_rows_decoded(const uint16_t *A, const double *Bd, void *C, int M, int N, int K,
+                             int out_dtype, const int64_t *rows, int64_t nrows, int nthreads);
+
 /*
  * Compute the listed rows of C.  `rows` holds nrows row indices into A;
  * output row r of C (nrows x N, packed) is row rows[r] of the product.
@@ -179,7 +182,28 @@ int oracle_gemm_rows(const uint16_t *A, const uint16_t *B, void *C, int M, int N
     double *Bd = (double *)malloc(sizeof(double) * (size_t)((int64_t)K * N > 0 ? (int64_t)K * N : 1));
     if (!Bd) return -2;
     if (K > 0) oracle_f16_decode_array(B, Bd, (int64_t)K * N);
+    int rc = oracle_gemm_rows_decoded(A, Bd, C, M, N, K, out_dtype, rows, nrows, nthreads);
+    free(Bd);
+    return rc;
+}
 
+/*
+ * As oracle_gemm_rows, with B already decoded to binary64 (K x N, e.g. by
+ * oracle_f16_decode_array), so that a caller computing many row samples of
+ * one product decodes B once.
+ */
+int oracle_gemm_rows_decoded(const uint16_t *A, const double *Bd, void *C, int M, int N, int K,
+                             int out_dtype, const int64_t *rows, int64_t nrows, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (out_dtype < 0 || out_dtype > 2) return -1;
+    if (nrows == 0 || N == 0) return 0;
+    if (!C || !rows) return -1;
+    if (K > 0 && (!A || !Bd)) return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > nrows) nthreads = (int)nrows;
     pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
     row_job *jobs = (row_job *)calloc((size_t)nthreads, sizeof(row_job));
     int rc = 0;
@@ -208,7 +232,6 @@ int oracle_gemm_rows(const uint16_t *A, const uint16_t *B, void *C, int M, int N
     }
     free(jobs);
     free(tids);
-    free(Bd);
     return rc;
 }
 

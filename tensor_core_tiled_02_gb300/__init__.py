@@ -1,0 +1,177 @@
+"""Python binding of the sm_103a pipelined tiled fp16 GEMM.
+
+Argument marshalling only: every step of the product runs in the CUDA
+library ``libtcgemm.so`` (built in-tree from ``csrc/`` by ``build.py``),
+reached through its C ABI (``include/gemm_f16.h``).  PyTorch supplies device
+memory and the current stream.  There is no fallback: if the library is
+missing the calls raise.
+
+Names follow the C ABI: ``gemm_f16`` (raw pointers), ``gemm_f16_plan``,
+``gemm_f16_set_config``, ``gemm_f16_strerror``, ``gemm_f16_device_status``;
+``matmul(a, b, out_dtype)`` is the tensor-level call of the quickstart's
+``matmul(a, b, out_dtype)``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtcgemm.so")
+
+GEMM_OUT_F16 = 0
+GEMM_OUT_F32 = 1
+
+STATUS = {
+    0: "GEMM_OK", -1: "GEMM_ERR_NULL", -2: "GEMM_ERR_DIM", -3: "GEMM_ERR_DTYPE",
+    -4: "GEMM_ERR_ALIGN", -5: "GEMM_ERR_ALIAS", -6: "GEMM_ERR_CONFIG", -7: "GEMM_ERR_TMAP",
+    -8: "GEMM_ERR_LAUNCH", -9: "GEMM_ERR_CUDA", -10: "GEMM_ERR_ARCH", -11: "GEMM_ERR_DEVICE_TIMEOUT",
+}
+EXPORTED = ["gemm_f16", "gemm_f16_plan", "gemm_f16_set_config", "gemm_f16_get_config",
+            "gemm_f16_strerror", "gemm_f16_device_status", "gemm_f16_abi_version"]
+
+
+class GemmPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "tile_m", "tile_n", "tile_k", "tiles_m", "tiles_n", "num_tiles", "k_steps", "stages",
+        "release", "grid", "raster_group", "smem_bytes", "tmem_cols", "threads")]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+class GemmConfig(ctypes.Structure):
+    _fields_ = [("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("release", ctypes.c_int),
+                ("grid", ctypes.c_int), ("raster_group", ctypes.c_int),
+                ("wait_limit", ctypes.c_longlong), ("inject_stall", ctypes.c_int)]
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, where: str = "gemm_f16"):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({strerror(code)})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the CUDA library (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with `python -m tensor_core_tiled_02_gb300.build` "
+                    "(there is no CPU fallback)")
+            lib = ctypes.CDLL(path)
+            vp, ci = ctypes.c_void_p, ctypes.c_int
+            lib.gemm_f16.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+            lib.gemm_f16.restype = ci
+            lib.gemm_f16_plan.argtypes = [ci, ci, ci, ci, ci, ctypes.POINTER(GemmPlan)]
+            lib.gemm_f16_plan.restype = ci
+            lib.gemm_f16_set_config.argtypes = [ctypes.POINTER(GemmConfig)]
+            lib.gemm_f16_set_config.restype = ci
+            lib.gemm_f16_get_config.argtypes = [ctypes.POINTER(GemmConfig)]
+            lib.gemm_f16_get_config.restype = ci
+            lib.gemm_f16_strerror.argtypes = [ci]
+            lib.gemm_f16_strerror.restype = ctypes.c_char_p
+            lib.gemm_f16_device_status.argtypes = [ctypes.POINTER(ci), ci]
+            lib.gemm_f16_device_status.restype = ci
+            lib.gemm_f16_abi_version.argtypes = []
+            lib.gemm_f16_abi_version.restype = ci
+            _lib = lib
+        return _lib
+
+
+def strerror(code: int) -> str:
+    return load_library().gemm_f16_strerror(int(code)).decode()
+
+
+def gemm_f16(A: int, B: int, C: int, M: int, N: int, K: int, out_dtype: int, stream: int = 0) -> int:
+    """The C entry point on raw device pointers (ints); returns its status code."""
+    return load_library().gemm_f16(A, B, C, M, N, K, out_dtype, stream)
+
+
+def gemm_f16_plan(M: int, N: int, K: int, out_dtype: int = GEMM_OUT_F16, num_sms: int = 0) -> dict:
+    p = GemmPlan()
+    rc = load_library().gemm_f16_plan(M, N, K, out_dtype, num_sms, ctypes.byref(p))
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_plan")
+    return p.as_dict()
+
+
+def gemm_f16_set_config(**fields) -> None:
+    """Set the tuning override; no arguments restores the defaults."""
+    cfg = GemmConfig()
+    for k, v in fields.items():
+        if not hasattr(cfg, k):
+            raise TypeError(f"unknown config field {k!r}")
+        setattr(cfg, k, int(v))
+    rc = load_library().gemm_f16_set_config(ctypes.byref(cfg) if fields else None)
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_set_config")
+
+
+def gemm_f16_get_config() -> dict:
+    cfg = GemmConfig()
+    rc = load_library().gemm_f16_get_config(ctypes.byref(cfg))
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_get_config")
+    return {n: getattr(cfg, n) for n, _ in cfg._fields_}
+
+
+def gemm_f16_device_status(reset: bool = True):
+    """(status code, wait site) after synchronising the current device."""
+    site = ctypes.c_int(0)
+    rc = load_library().gemm_f16_device_status(ctypes.byref(site), int(bool(reset)))
+    return rc, site.value
+
+
+def _out_code(out_dtype) -> int:
+    import torch
+
+    if out_dtype in (torch.float16, GEMM_OUT_F16):
+        return GEMM_OUT_F16
+    if out_dtype in (torch.float32, GEMM_OUT_F32):
+        return GEMM_OUT_F32
+    raise ValueError(f"out_dtype must be torch.float16 or torch.float32, got {out_dtype}")
+
+
+def matmul(a, b, out_dtype=None, out=None, stream=None):
+    """C = a @ b for fp16 CUDA tensors a [M, K] and b [K, N]; C is fp16 (default) or fp32.
+
+    The kernel is enqueued on ``stream`` (default: torch's current stream) and
+    the call returns without synchronising.  Raises ``GemmError`` on a nonzero
+    status from the library and ``ValueError`` on tensors it cannot take.
+    """
+    import torch
+
+    if out_dtype is None:
+        out_dtype = torch.float16
+    code = _out_code(out_dtype)
+    tdt = torch.float16 if code == GEMM_OUT_F16 else torch.float32
+    if a.dtype != torch.float16 or b.dtype != torch.float16:
+        raise ValueError("a and b must be torch.float16")
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError(f"shape mismatch: {tuple(a.shape)} @ {tuple(b.shape)}")
+    if not (a.is_cuda and b.is_cuda):
+        raise ValueError("a and b must be CUDA tensors")
+    if not (a.is_contiguous() and b.is_contiguous()):
+        raise ValueError("a and b must be contiguous row-major")
+    M, K = a.shape
+    N = b.shape[1]
+    if out is None:
+        out = torch.empty((M, N), dtype=tdt, device=a.device)
+    elif out.dtype != tdt or tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] tensor of out_dtype")
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(a.device):
+        rc = gemm_f16(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, code, handle)
+    if rc != 0:
+        raise GemmError(rc)
+    return out

@@ -1,0 +1,336 @@
+// Host side of the fp16 GEMM: argument checks, the planner, tensor-map
+// encoding and the launch.  The C ABI is declared in include/gemm_f16.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_f16.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using namespace tcgemm;
+
+constexpr int kMaxDevices = 64;
+constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_100-class parts
+constexpr long long kDefaultWaitLimit = 2000000000LL;  // ~1 s at 2 GHz
+
+std::mutex g_mu;
+gemm_config g_cfg = {};
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int cc = 0;
+    bool attr_set[2][2] = {{false, false}, {false, false}};  // [tile_n == 256][out_dtype]
+};
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int out_bytes(int out_dtype) { return out_dtype == GEMM_OUT_F16 ? 2 : 4; }
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Argument checks that need no CUDA.  Returns GEMM_OK, or 1 for "nothing to do".
+int check_args(const void* A, const void* B, const void* C, int M, int N, int K, int out_dtype, bool check_ptrs) {
+    if (out_dtype != GEMM_OUT_F16 && out_dtype != GEMM_OUT_F32) return GEMM_ERR_DTYPE;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_DIM;
+    if (N % 8 != 0 || K % 8 != 0) return GEMM_ERR_ALIGN;
+    // tile ids and tile coordinates must fit an int
+    if ((long long)ceil_div(M, kBM) * ceil_div(N, 128) > INT_MAX) return GEMM_ERR_DIM;
+    if (M == 0 || N == 0) return 1;
+    if (!check_ptrs) return GEMM_OK;
+    if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_NULL;
+    const uintptr_t a = (uintptr_t)A, b = (uintptr_t)B, c = (uintptr_t)C;
+    if ((c & 15) || (K > 0 && ((a & 15) || (b & 15)))) return GEMM_ERR_ALIGN;
+    if (K > 0) {
+        // inputs read-only, output write-only: C may not overlap A or B
+        const uint64_t c_end = c + (uint64_t)M * N * out_bytes(out_dtype);
+        const uint64_t a_end = a + (uint64_t)M * K * 2;
+        const uint64_t b_end = b + (uint64_t)K * N * 2;
+        if (c < a_end && a < c_end) return GEMM_ERR_ALIAS;
+        if (c < b_end && b < c_end) return GEMM_ERR_ALIAS;
+    }
+    return GEMM_OK;
+}
+
+int check_config(const gemm_config& c) {
+    if (c.tile_n != 0 && c.tile_n != 128 && c.tile_n != 256) return GEMM_ERR_CONFIG;
+    if (c.stages < 0 || c.stages > kMaxStages) return GEMM_ERR_CONFIG;
+    if (c.release < 0 || c.release >= kMaxStages) return GEMM_ERR_CONFIG;
+    if (c.stages != 0 && c.release >= c.stages) return GEMM_ERR_CONFIG;
+    if (c.grid < 0 || c.raster_group < 0 || c.wait_limit < 0) return GEMM_ERR_CONFIG;
+    if (c.inject_stall != 0 && c.inject_stall != 1) return GEMM_ERR_CONFIG;
+    return GEMM_OK;
+}
+
+int smem_for(int tile_n, int out_dtype, int stages) {
+    if (tile_n == 256)
+        return out_dtype == GEMM_OUT_F16 ? Layout<256, 0>::smem_bytes(stages) : Layout<256, 1>::smem_bytes(stages);
+    return out_dtype == GEMM_OUT_F16 ? Layout<128, 0>::smem_bytes(stages) : Layout<128, 1>::smem_bytes(stages);
+}
+
+int max_stages_for(int tile_n, int out_dtype) {
+    int s = kMaxStages;
+    while (s > 1 && smem_for(tile_n, out_dtype, s) > kSmemLimit) --s;
+    return s;
+}
+
+// The planner.  Tile: 128 x 256 when there are at least as many such tiles as
+// SMs, else 128 x 128 (more tiles for small or skinny problems).  Ring depth:
+// the deepest that fits shared memory, clamped to the steps one CTA runs
+// (emit_pipeline clamps max_concurrent_steps to the grid the same way), and
+// always above the release depth.
+int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config& cfg, gemm_plan* p) {
+    std::memset(p, 0, sizeof(*p));
+    p->tile_m = kBM;
+    p->tile_k = kBK;
+    int tn = cfg.tile_n;
+    if (tn == 0) {
+        const long long tiles256 = (long long)ceil_div(M, kBM) * ceil_div(N, 256);
+        tn = tiles256 >= num_sms ? 256 : 128;
+    }
+    p->tile_n = tn;
+    p->tiles_m = ceil_div(M, kBM);
+    p->tiles_n = ceil_div(N, tn);
+    p->num_tiles = p->tiles_m * p->tiles_n;
+    p->k_steps = ceil_div(K, kBK);
+    p->grid = p->num_tiles < num_sms ? p->num_tiles : num_sms;
+    if (cfg.grid > 0 && cfg.grid < p->grid) p->grid = cfg.grid;
+    if (p->grid < 1) p->grid = 1;
+    p->release = cfg.release;
+    const int max_s = max_stages_for(tn, out_dtype);
+    int s = cfg.stages > 0 ? cfg.stages : max_s;
+    if (s > max_s) return GEMM_ERR_CONFIG;
+    if (p->release >= s) return GEMM_ERR_CONFIG;
+    const long long steps_per_cta = (long long)p->k_steps * ceil_div(p->num_tiles, p->grid);
+    if (steps_per_cta < s) s = (int)(steps_per_cta > p->release ? steps_per_cta : p->release + 1);
+    if (s < 1) s = 1;
+    p->stages = s;
+    p->raster_group = cfg.raster_group > 0 ? cfg.raster_group : 8;
+    p->smem_bytes = smem_for(tn, out_dtype, s);
+    p->tmem_cols = 2 * tn;
+    p->threads = kThreads;
+    return GEMM_OK;
+}
+
+void init_encode() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+}
+
+// 2-D row-major tensor map with a 128-byte swizzle; out-of-range elements
+// read as zero and are not written.
+int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr, uint64_t inner,
+              uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TMAP;
+}
+
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        int sms = 0, major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        d.sms = sms;
+        d.cc = major * 10 + minor;
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+template <int BN, int OUT>
+int launch(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+           const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
+    auto kern = gemm_f16_kernel<BN, OUT>;
+    bool& attr = dev.attr_set[BN == 256][OUT];
+    if (!attr) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        attr = true;
+    }
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(plan.grid, 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = plan.smem_bytes;
+    lc.stream = stream;
+    cudaError_t e = cudaLaunchKernelEx(&lc, kern, ta, tb, tc, kp);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype,
+             gemm_stream_t stream) {
+    int rc = check_args(A, B, C, M, N, K, out_dtype, true);
+    if (rc == 1) return GEMM_OK;
+    if (rc != GEMM_OK) return rc;
+    gemm_config cfg;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        cfg = g_cfg;
+    }
+    DeviceInfo* dev = nullptr;
+    rc = device_info(&dev);
+    if (rc != GEMM_OK) return rc;
+    if (dev->cc != 103) return GEMM_ERR_ARCH;
+    gemm_plan plan;
+    rc = plan_impl(M, N, K, out_dtype, dev->sms, cfg, &plan);
+    if (rc != GEMM_OK) return rc;
+
+    std::call_once(g_encode_once, init_encode);
+    if (!g_encode) return GEMM_ERR_CUDA;
+    CUtensorMap ta, tb, tc;
+    std::memset(&ta, 0, sizeof(ta));
+    std::memset(&tb, 0, sizeof(tb));
+    if (K > 0) {
+        rc = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, kBK, kBM);
+        if (rc != GEMM_OK) return rc;
+        rc = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK);
+        if (rc != GEMM_OK) return rc;
+    }
+    if (out_dtype == GEMM_OUT_F16)
+        rc = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, C, (uint64_t)N, (uint64_t)M, 64, 32);
+    else
+        rc = encode_2d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, (uint64_t)N, (uint64_t)M, 32, 32);
+    if (rc != GEMM_OK) return rc;
+
+    KernelParams kp;
+    kp.M = M;
+    kp.N = N;
+    kp.K = K;
+    kp.tiles_m = plan.tiles_m;
+    kp.tiles_n = plan.tiles_n;
+    kp.k_blocks = plan.k_steps;
+    kp.raster_group = plan.raster_group;
+    kp.stages = plan.stages;
+    kp.release = plan.release;
+    kp.wait_limit = cfg.wait_limit > 0 ? cfg.wait_limit : kDefaultWaitLimit;
+    kp.inject = cfg.inject_stall;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan.tile_n == 256)
+        return out_dtype == GEMM_OUT_F16 ? launch<256, 0>(plan, ta, tb, tc, kp, s, *dev)
+                                         : launch<256, 1>(plan, ta, tb, tc, kp, s, *dev);
+    return out_dtype == GEMM_OUT_F16 ? launch<128, 0>(plan, ta, tb, tc, kp, s, *dev)
+                                     : launch<128, 1>(plan, ta, tb, tc, kp, s, *dev);
+}
+
+int gemm_f16_plan(int M, int N, int K, int out_dtype, int num_sms, gemm_plan* out) {
+    if (!out) return GEMM_ERR_NULL;
+    int rc = check_args(nullptr, nullptr, nullptr, M, N, K, out_dtype, false);
+    if (rc < 0) return rc;
+    if (num_sms < 0) return GEMM_ERR_DIM;
+    if (num_sms == 0) {
+        DeviceInfo* dev = nullptr;
+        rc = device_info(&dev);
+        if (rc != GEMM_OK) return rc;
+        num_sms = dev->sms;
+    }
+    gemm_config cfg;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        cfg = g_cfg;
+    }
+    return plan_impl(M, N, K, out_dtype, num_sms, cfg, out);
+}
+
+int gemm_f16_set_config(const gemm_config* cfg) {
+    gemm_config c = {};
+    if (cfg) c = *cfg;
+    int rc = check_config(c);
+    if (rc != GEMM_OK) return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_cfg = c;
+    return GEMM_OK;
+}
+
+int gemm_f16_get_config(gemm_config* out) {
+    if (!out) return GEMM_ERR_NULL;
+    std::lock_guard<std::mutex> lk(g_mu);
+    *out = g_cfg;
+    return GEMM_OK;
+}
+
+const char* gemm_f16_strerror(int code) {
+    switch (code) {
+        case GEMM_OK: return "success";
+        case GEMM_ERR_NULL: return "a required pointer is NULL";
+        case GEMM_ERR_DIM: return "M, N or K is negative or the problem is too large to index";
+        case GEMM_ERR_DTYPE: return "out_dtype must be GEMM_OUT_F16 (0) or GEMM_OUT_F32 (1)";
+        case GEMM_ERR_ALIGN: return "pointers must be 16-byte aligned and N, K multiples of 8";
+        case GEMM_ERR_ALIAS: return "C overlaps A or B";
+        case GEMM_ERR_CONFIG: return "invalid tuning config (release must be < stages; tile_n 128 or 256)";
+        case GEMM_ERR_TMAP: return "the driver refused a TMA tensor-map encoding";
+        case GEMM_ERR_LAUNCH: return "kernel launch failed";
+        case GEMM_ERR_CUDA: return "no usable CUDA device or driver";
+        case GEMM_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel's bounded device-side wait ran out";
+        default: return "unknown gemm_status code";
+    }
+}
+
+int gemm_f16_device_status(int* site, int reset) {
+    if (site) *site = 0;
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != GEMM_OK) return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (reset && v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+    }
+    if (site) *site = (int)v;
+    return v == 0 ? GEMM_OK : GEMM_ERR_DEVICE_TIMEOUT;
+}
+
+int gemm_f16_abi_version(void) { return 1; }
+
+}  // extern "C"

@@ -12,15 +12,22 @@ check rides along, derived from the arithmetic:
     C - C_ref over the elements is about one fp16 half-ulp of the typical
     |C|, i.e. 2^-11 |C| / sqrt(3) ~ 3e-4 |C|; a bound of 2e-3 rms(C_ref)
     catches a lost K-block (one of 64 dropped gives 0.125 rms(C_ref)).
-  * fp32 output: the fp32 accumulation error of a sum of K products grows
-    like sqrt(K) 2^-24 rms(C) at most a few times over, far below 1e-5
-    rms(C_ref) at K = 32768; the bound is 1e-5 rms(C_ref).
+  * fp32 output: only the accumulation errs.  The tensor core adds each
+    group of 16 products (one tcgen05.mma K slice) to the fp32 accumulator
+    with truncating alignment rather than IEEE round-to-nearest per add, so
+    the error may grow linearly in the number of groups, not as sqrt(K).
+    Bound: 2 fp32 ulps (2^-22 relative) per group, with a floor of 8 groups:
+    rms(C - C_ref) <= 2^-22 (K/16 + 8) rms(C_ref).  At K = 32768 that is
+    4.9e-4, still 90 times below the 4.4e-2 a single lost K-block gives.
 """
 from __future__ import annotations
 
 import numpy as np
 
-RMS_BOUND = {0: 2e-3, 1: 1e-5}
+
+def rms_bound(out_dtype: int, K: int) -> float:
+    acc = 2.0 ** -22 * (K / 16.0 + 8.0)
+    return 2e-3 + acc if out_dtype == 0 else acc
 
 
 def tolerance(c_ref: np.ndarray, K: int) -> np.ndarray:
@@ -48,5 +55,5 @@ def check(c_gpu: np.ndarray, c_ref: np.ndarray, K: int, out_dtype: int, what: st
     diag = {"n": int(c_ref.size), "max_abs_err": float(err.max()),
             "rms_err_over_rms_ref": err_rms / ref_rms if ref_rms > 0 else err_rms}
     if ref_rms > 0:
-        assert err_rms <= RMS_BOUND[out_dtype] * ref_rms, f"{what}: rms error too large: {diag}"
+        assert err_rms <= rms_bound(out_dtype, K) * ref_rms, f"{what}: rms error too large: {diag}"
     return diag

@@ -1,0 +1,248 @@
+"""Parity of the CUDA path with the CPU oracle, element by element.
+
+Small and mid-size problems (several tiles, ragged tails in M, N and K) are
+checked whole; the five workloads at full size, in the launch configuration
+the bench times, on sampled rows and elements the oracle computes one by one.
+Bit-exact properties (all-ones, identity, permutation, determinism, zero
+padding) are checked where the arithmetic makes them exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import parity
+import tensor_core_tiled_02_gb300 as tc
+from tensor_core_tiled_02_gb300.synthetic import WORKLOADS, draw, make_inputs, workload_inputs
+
+torch = pytest.importorskip("torch")
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA device")]
+
+
+@pytest.fixture(autouse=True)
+def _clean_state():
+    tc.gemm_f16_set_config()
+    yield
+    tc.gemm_f16_set_config()
+    rc, site = tc.gemm_f16_device_status(reset=True)
+    assert rc == 0, f"a device wait gave up (site {site})"
+
+
+def gpu_gemm(a, b, out_dtype):
+    """Run the CUDA path on CPU fp16 tensors; return the result on the CPU."""
+    a_d = a.cuda()
+    b_d = b.cuda()
+    c = tc.matmul(a_d, b_d, out_dtype=torch.float16 if out_dtype == 0 else torch.float32)
+    torch.cuda.synchronize()
+    return c.cpu()
+
+
+def values(c):
+    return c.double().numpy()
+
+
+def oracle_rows(a, b, out_dtype, rows=None):
+    c = oracle.gemm(a.numpy(), b.numpy(), out_dtype, rows=rows)
+    return oracle.as_values(c, out_dtype)
+
+
+def check_full(a, b, out_dtype, what):
+    c = gpu_gemm(a, b, out_dtype)
+    ref = oracle_rows(a, b, out_dtype)
+    return parity.check(values(c), ref, a.shape[1], out_dtype, what), c
+
+
+# ---- whole-matrix parity ------------------------------------------------------
+
+
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_workload_256_whole(out_dtype):
+    w = WORKLOADS["gemm_256"]
+    a, b = workload_inputs(w)
+    check_full(a, b, out_dtype, "gemm_256")
+
+
+RAGGED = [(300, 392, 520), (129, 136, 72), (1, 8, 8), (127, 264, 1000), (515, 1000, 64), (64, 2056, 200)]
+
+
+@pytest.mark.parametrize("M,N,K", RAGGED)
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_ragged_shapes(M, N, K, out_dtype):
+    a, b = make_inputs(M, N, K, ("normal", 1.0), ("normal", 0.5), seed_a=M, seed_b=N + K)
+    check_full(a, b, out_dtype, f"ragged {M}x{N}x{K}")
+
+
+VARIANTS = [dict(tile_n=t, stages=s, release=r)
+            for t in (128, 256) for s in (1, 2, 3, 4) for r in (0, 1, 2) if r < s]
+
+
+@pytest.mark.parametrize("cfg", VARIANTS, ids=lambda c: f"n{c['tile_n']}s{c['stages']}r{c['release']}")
+def test_pipeline_variants(cfg):
+    """Every tile shape, ring depth and release depth the tuner may pick."""
+    tc.gemm_f16_set_config(**cfg)
+    a, b = make_inputs(300, 520, 776, ("uniform", 1.0), ("uniform", 1.0), seed_a=5, seed_b=6)
+    for out_dtype in (0, 1):
+        check_full(a, b, out_dtype, f"variant {cfg} out {out_dtype}")
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_persistent_many_tiles_per_cta(tile_n):
+    """A handful of CTAs each walk many tiles: the ring and both TMEM
+    accumulators wrap many times across tile boundaries."""
+    tc.gemm_f16_set_config(tile_n=tile_n, grid=3, raster_group=3)
+    a, b = make_inputs(1100, 1024, 264, ("uniform", 1.0), ("uniform", 1.0), seed_a=9, seed_b=10)
+    check_full(a, b, 0, f"persistent tile_n={tile_n}")
+
+
+def test_subnormal_and_scaled_inputs():
+    # N(0,1)/64 inputs put ~0.3% of entries in the fp16 subnormal range
+    a = draw((384, 512), ("normal", 1 / 64), 3)
+    b = draw((512, 256), ("normal", 1 / 64), 4)
+    assert ((a.abs() < 2 ** -14) & (a != 0)).any()
+    check_full(a, b, 0, "subnormals")
+    check_full(a, b, 1, "subnormals f32")
+
+
+# ---- degenerate sizes -------------------------------------------------------------
+
+
+def test_k_zero_writes_zeros():
+    a = torch.zeros((200, 0), dtype=torch.float16, device="cuda")
+    b = torch.zeros((0, 136), dtype=torch.float16, device="cuda")
+    for dt in (torch.float16, torch.float32):
+        c = torch.full((200, 136), 7.0, dtype=dt, device="cuda")
+        tc.matmul(a, b, out_dtype=dt, out=c)
+        torch.cuda.synchronize()
+        assert not c.any()
+
+
+def test_empty_outputs():
+    a = torch.zeros((0, 64), dtype=torch.float16, device="cuda")
+    b = torch.ones((64, 128), dtype=torch.float16, device="cuda")
+    assert tc.matmul(a, b).shape == (0, 128)
+    a = torch.ones((64, 64), dtype=torch.float16, device="cuda")
+    b = torch.ones((64, 0), dtype=torch.float16, device="cuda")
+    assert tc.matmul(a, b).shape == (64, 0)
+
+
+def test_errors_with_real_pointers():
+    a = torch.ones((256, 256), dtype=torch.float16, device="cuda")
+    b = torch.ones((256, 256), dtype=torch.float16, device="cuda")
+    # C on top of A
+    rc = tc.gemm_f16(a.data_ptr(), b.data_ptr(), a.data_ptr(), 256, 256, 256, 0, 0)
+    assert rc == -5
+    # misaligned pointer (2 bytes in)
+    rc = tc.gemm_f16(a.data_ptr() + 2, b.data_ptr(), torch.empty_like(a).data_ptr(), 128, 128, 128, 0, 0)
+    assert rc == -4
+
+
+# ---- bit-exact properties on the GPU ---------------------------------------------
+
+
+@pytest.mark.parametrize("K", [256, 4096, 8192, 32768])
+def test_all_ones_exact(K):
+    """All-ones A and B give C = K exactly (fp32 sums of ones are exact below 2^24)."""
+    a = torch.ones((256, K), dtype=torch.float16, device="cuda")
+    b = torch.ones((K, 256), dtype=torch.float16, device="cuda")
+    for dt in (torch.float16, torch.float32):
+        c = tc.matmul(a, b, out_dtype=dt)
+        torch.cuda.synchronize()
+        assert bool((c == K).all()), (K, dt)
+
+
+def test_identity_returns_a_bit_exact():
+    a = draw((384, 512), ("normal", 1.0), 11)
+    a[a == 0] = 0  # -0 sums to +0, as in the oracle
+    eye = torch.eye(512, dtype=torch.float16)
+    c = gpu_gemm(a, eye, 0)
+    assert torch.equal(c.view(torch.int16), a.view(torch.int16))
+    c32 = gpu_gemm(a, eye, 1)
+    assert torch.equal(c32, a.float())
+
+
+def test_row_permutation_and_determinism():
+    """Permuting rows of A permutes rows of C bit for bit (each element's
+    K order is fixed), and two runs agree bit for bit."""
+    a, b = make_inputs(640, 768, 1024, ("uniform", 1.0), ("uniform", 1.0), seed_a=21, seed_b=22)
+    c1 = gpu_gemm(a, b, 1)
+    c2 = gpu_gemm(a, b, 1)
+    assert torch.equal(c1.view(torch.int32), c2.view(torch.int32))
+    perm = torch.randperm(640, generator=torch.Generator().manual_seed(0))
+    cp = gpu_gemm(a[perm].contiguous(), b, 1)
+    assert torch.equal(cp.view(torch.int32), c1[perm].view(torch.int32))
+
+
+def test_zero_padding_in_k_is_invariant():
+    a, b = make_inputs(256, 256, 200, ("uniform", 1.0), ("uniform", 1.0), seed_a=31, seed_b=32)
+    ap = torch.zeros((256, 256), dtype=torch.float16)
+    ap[:, :200] = a
+    bp = torch.zeros((256, 256), dtype=torch.float16)
+    bp[:200] = b
+    c = gpu_gemm(a, b, 1)
+    cpad = gpu_gemm(ap, bp, 1)
+    assert torch.equal(c.view(torch.int32), cpad.view(torch.int32))
+
+
+def test_transpose_identity():
+    """(A B)^T = B^T A^T, within the tolerance (the K order may differ)."""
+    a, b = make_inputs(384, 256, 512, ("uniform", 1.0), ("uniform", 1.0), seed_a=41, seed_b=42)
+    c = gpu_gemm(a, b, 1)
+    ct = gpu_gemm(b.t().contiguous(), a.t().contiguous(), 1)
+    ref = values(c).T
+    parity.check(values(ct), ref, 512, 1, "transpose")
+
+
+# ---- the five workloads at full size, sampled ----------------------------------
+
+
+def sampled_rows(M, tile=128, n_random=24, seed=0):
+    rng = np.random.default_rng(seed)
+    fixed = {0, 1, min(tile - 1, M - 1), min(tile, M - 1), M - 1, max(M - tile, 0)}
+    rnd = set(rng.integers(0, M, n_random).tolist())
+    return np.array(sorted(fixed | rnd), np.int64)
+
+
+@pytest.mark.parametrize("name", ["gemm_4096", "gemm_8192", "skinny", "long_k"])
+def test_workload_full_size_sampled(name):
+    w = WORKLOADS[name]
+    a, b = workload_inputs(w)
+    c = gpu_gemm(a, b, w.out_dtype)
+    rows = sampled_rows(w.M)
+    ref = oracle_rows(a, b, w.out_dtype, rows=rows)
+    diag = parity.check(values(c)[rows], ref, w.K, w.out_dtype, f"{name} rows")
+    # plus scattered single elements over the whole output
+    rng = np.random.default_rng(1)
+    ii = rng.integers(0, w.M, 2048)
+    jj = rng.integers(0, w.N, 2048)
+    e = oracle.as_values(oracle.gemm_elems(a.numpy(), b.numpy(), ii, jj, w.out_dtype), w.out_dtype)
+    parity.check(values(c)[ii, jj], e, w.K, w.out_dtype, f"{name} elements")
+    print(name, diag)
+
+
+def test_skinny_whole():
+    """The memory-bound workload is small enough for the oracle to check whole."""
+    w = WORKLOADS["skinny"]
+    a, b = workload_inputs(w)
+    check_full(a, b, w.out_dtype, "skinny whole")
+
+
+# ---- the device-side timeout path ----------------------------------------------------
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """With the test hook set, no operand is ever loaded: the MMA warp's
+    bounded wait runs out (~10 ms), the kernel winds down and reports the
+    timeout, and the context stays usable for a normal call afterwards."""
+    a, b = make_inputs(256, 256, 256, ("uniform", 1.0), ("uniform", 1.0))
+    a_d, b_d = a.cuda(), b.cuda()
+    tc.gemm_f16_set_config(inject_stall=1, wait_limit=20_000_000)
+    tc.matmul(a_d, b_d)
+    rc, site = tc.gemm_f16_device_status(reset=True)
+    assert rc == -11 and site == 2, (rc, site)
+    tc.gemm_f16_set_config()
+    rc, site = tc.gemm_f16_device_status(reset=True)
+    assert rc == 0 and site == 0
+    c = tc.matmul(a_d, b_d)
+    torch.cuda.synchronize()
+    parity.check(values(c.cpu()), oracle_rows(a, b, 0), 256, 0, "after timeout")
