@@ -1,17 +1,18 @@
 /*
  * gemm_f16.h - C ABI of the GB300 (sm_103a) pipelined tiled fp16 GEMM.
  *
- * The operation is the matmul of the "JAX Pallas Mosaic GPU quickstart",
- * section "Hopper matrix multiplication kernel": matmul(a, b, out_dtype)
+ * The operation is the matmul of "Quickstart: GPU" (Pallas Mosaic GPU),
+ * section "Pipelining: a matmul kernel": matmul(a, b, out_dtype)
  * with m, k = a.shape and _, n = b.shape, fp16 operands, an fp32 Tensor Core
  * accumulator (plgpu.ACC) and a final conversion acc.astype(out_dtype):
  *
  *     C[i][j] = out_dtype( sum_k  A[i][k] * B[k][j] ),  accumulated in fp32.
  *
  * The parallel grid of output tiles, the sequential pipeline along K and its
- * two knobs (max_concurrent_steps, delay_release) come from the same page's
- * "Key emit_pipeline parameters" section and from the "Pallas software
- * pipelining guide" (sections 3, 4 and 9.2).  Here they are realised with TMA,
+ * two knobs (max_concurrent_steps, delay_release) come from the same page,
+ * from "JAX Pallas Mosaic GPU 快速上手" (section "深入emit_pipeline的关键参数")
+ * and from "JAX Pallas 软件流水线 Software Pipelining 完全指南" (sections 3,
+ * 4 and 9.2).  Here they are realised with TMA,
  * an mbarrier-guarded shared-memory ring, tcgen05.mma into Tensor Memory and
  * a persistent tile scheduler.
  *
@@ -66,8 +67,9 @@ typedef struct {
     int tiles_m, tiles_n;       /* ceil(M/tile_m), ceil(N/tile_n) */
     int num_tiles;              /* tiles_m * tiles_n: one owner CTA each */
     int k_steps;                /* ceil(K/tile_k): the sequential pipeline length */
-    int stages;                 /* shared-memory ring depth (max_concurrent_steps) */
-    int release;                /* extra buffer-release depth (delay_release) */
+    int stages;                 /* loads in flight ahead of the MMA (max_concurrent_steps) */
+    int release;                /* extra steps before a buffer is reused (delay_release) */
+    int slots;                  /* shared-memory ring buffers: stages + release */
     int grid;                   /* persistent CTAs launched */
     int raster_group;           /* m-blocks per raster group */
     int smem_bytes;             /* dynamic shared memory per CTA */
@@ -78,8 +80,9 @@ typedef struct {
 /* Tuning override.  Zero in a field means "planner default". */
 typedef struct {
     int tile_n;            /* 0, 128 or 256 */
-    int stages;            /* 0 or 1..8 */
-    int release;           /* 0..7, must be < the stages used */
+    int stages;            /* 0 or 1..8: loads in flight (max_concurrent_steps) */
+    int release;           /* 0..7: delay_release; stages must exceed it, and
+                              stages + release buffers must fit shared memory */
     int grid;              /* 0 = min(num_tiles, SM count); else a cap on the CTAs launched */
     int raster_group;      /* 0 or >= 1 */
     long long wait_limit;  /* 0 = about one second; else clock cycles one device wait may take */

@@ -7,10 +7,9 @@ and the two share no code.
 
 The arithmetic lives in ``gemm_oracle.c`` (plain C, fp64 accumulation, its own
 binary16 codec); this module only compiles it with gcc and marshals numpy
-arrays through ctypes.  What it computes follows "JAX Pallas Mosaic GPU
-quickstart", section "Hopper matrix multiplication kernel":
-``matmul(a, b, out_dtype)`` with an fp32 accumulator and ``astype(out_dtype)``,
-checked there against the untiled ``a @ b``.  The oracle is that untiled
+arrays through ctypes.  What it computes follows "Quickstart: GPU", section
+"Pipelining: a matmul kernel": ``matmul(a, b, out_dtype)`` with an fp32
+accumulator and ``astype(out_dtype)``, checked against the untiled ``a @ b``.  The oracle is that untiled
 product in fp64, rounded once to the output type.
 """
 from __future__ import annotations

@@ -7,11 +7,12 @@
  * header or table with the CUDA path.
  *
  * What it computes (the plain definition the tiled kernel must reach):
- *   "JAX Pallas Mosaic GPU quickstart", section "Hopper matrix
- *   multiplication kernel": matmul(a, b, out_dtype) with a:[m,k], b:[k,n]
- *   fp16, an fp32 Tensor Core accumulator (plgpu.ACC), and a final
- *   acc.astype(out_dtype).  The same page checks its pipelined kernels with
- *   assert_allclose(result, a @ b), i.e. against the untiled product.
+ *   "Quickstart: GPU", section "Pipelining: a matmul kernel":
+ *   matmul(a, b, out_dtype) with a:[m,k], b:[k,n] fp16, an fp32 Tensor Core
+ *   accumulator (plgpu.ACC), and a final acc.astype(out_dtype).  The page
+ *   "JAX Pallas Mosaic GPU 快速上手" (section "与仓库实现的对应关系") notes the
+ *   pipelined kernels are checked with assert_allclose(result, a @ b), i.e.
+ *   against the untiled product.
  *
  *   C_ref[i][j] = round_out( sum_{k=0..K-1} f64(A[i][k]) * f64(B[k][j]) )
  *

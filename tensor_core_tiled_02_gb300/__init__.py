@@ -8,8 +8,8 @@ missing the calls raise.
 
 Names follow the C ABI: ``gemm_f16`` (raw pointers), ``gemm_f16_plan``,
 ``gemm_f16_set_config``, ``gemm_f16_strerror``, ``gemm_f16_device_status``;
-``matmul(a, b, out_dtype)`` is the tensor-level call of the quickstart's
-``matmul(a, b, out_dtype)``.
+``matmul(a, b, out_dtype)`` is the tensor-level call of the ``matmul(a, b,
+out_dtype)`` of "Quickstart: GPU", section "Pipelining: a matmul kernel".
 """
 from __future__ import annotations
 
@@ -35,7 +35,7 @@ EXPORTED = ["gemm_f16", "gemm_f16_plan", "gemm_f16_set_config", "gemm_f16_get_co
 class GemmPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "tile_m", "tile_n", "tile_k", "tiles_m", "tiles_n", "num_tiles", "k_steps", "stages",
-        "release", "grid", "raster_group", "smem_bytes", "tmem_cols", "threads")]
+        "release", "slots", "grid", "raster_group", "smem_bytes", "tmem_cols", "threads")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -66,28 +66,32 @@ int check_config(const gemm_config& c) {
     if (c.stages < 0 || c.stages > kMaxStages) return GEMM_ERR_CONFIG;
     if (c.release < 0 || c.release >= kMaxStages) return GEMM_ERR_CONFIG;
     if (c.stages != 0 && c.release >= c.stages) return GEMM_ERR_CONFIG;
+    if (c.stages + c.release > kMaxStages) return GEMM_ERR_CONFIG;
     if (c.grid < 0 || c.raster_group < 0 || c.wait_limit < 0) return GEMM_ERR_CONFIG;
     if (c.inject_stall != 0 && c.inject_stall != 1) return GEMM_ERR_CONFIG;
     return GEMM_OK;
 }
 
-int smem_for(int tile_n, int out_dtype, int stages) {
+int smem_for(int tile_n, int out_dtype, int slots) {
     if (tile_n == 256)
-        return out_dtype == GEMM_OUT_F16 ? Layout<256, 0>::smem_bytes(stages) : Layout<256, 1>::smem_bytes(stages);
-    return out_dtype == GEMM_OUT_F16 ? Layout<128, 0>::smem_bytes(stages) : Layout<128, 1>::smem_bytes(stages);
+        return out_dtype == GEMM_OUT_F16 ? Layout<256, 0>::smem_bytes(slots) : Layout<256, 1>::smem_bytes(slots);
+    return out_dtype == GEMM_OUT_F16 ? Layout<128, 0>::smem_bytes(slots) : Layout<128, 1>::smem_bytes(slots);
 }
 
-int max_stages_for(int tile_n, int out_dtype) {
+int max_slots_for(int tile_n, int out_dtype) {
     int s = kMaxStages;
     while (s > 1 && smem_for(tile_n, out_dtype, s) > kSmemLimit) --s;
     return s;
 }
 
 // The planner.  Tile: 128 x 256 when there are at least as many such tiles as
-// SMs, else 128 x 128 (more tiles for small or skinny problems).  Ring depth:
-// the deepest that fits shared memory, clamped to the steps one CTA runs
-// (emit_pipeline clamps max_concurrent_steps to the grid the same way), and
-// always above the release depth.
+// SMs, else 128 x 128 (more tiles for small or skinny problems).
+// Pipeline depth, in the pages' terms: `stages` (max_concurrent_steps) loads in
+// flight ahead of the MMA and `release` (delay_release) extra steps before a
+// buffer is handed back, so the ring holds stages + release buffers.  As in
+// emit_pipeline, stages must exceed release, and stages is clamped to the
+// steps one CTA runs (never below release + 1).  Default: the deepest ring
+// that fits shared memory.
 int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config& cfg, gemm_plan* p) {
     std::memset(p, 0, sizeof(*p));
     p->tile_m = kBM;
@@ -105,17 +109,18 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
     p->grid = p->num_tiles < num_sms ? p->num_tiles : num_sms;
     if (cfg.grid > 0 && cfg.grid < p->grid) p->grid = cfg.grid;
     if (p->grid < 1) p->grid = 1;
-    p->release = cfg.release;
-    const int max_s = max_stages_for(tn, out_dtype);
-    int s = cfg.stages > 0 ? cfg.stages : max_s;
-    if (s > max_s) return GEMM_ERR_CONFIG;
-    if (p->release >= s) return GEMM_ERR_CONFIG;
+    const int d = cfg.release;
+    const int max_slots = max_slots_for(tn, out_dtype);
+    int s = cfg.stages > 0 ? cfg.stages : max_slots - d;
+    if (s <= d) return GEMM_ERR_CONFIG;
+    if (s + d > max_slots) return GEMM_ERR_CONFIG;
     const long long steps_per_cta = (long long)p->k_steps * ceil_div(p->num_tiles, p->grid);
-    if (steps_per_cta < s) s = (int)(steps_per_cta > p->release ? steps_per_cta : p->release + 1);
-    if (s < 1) s = 1;
+    if (steps_per_cta < s) s = (int)(steps_per_cta > d ? steps_per_cta : d + 1);
     p->stages = s;
+    p->release = d;
+    p->slots = s + d;
     p->raster_group = cfg.raster_group > 0 ? cfg.raster_group : 8;
-    p->smem_bytes = smem_for(tn, out_dtype, s);
+    p->smem_bytes = smem_for(tn, out_dtype, p->slots);
     p->tmem_cols = 2 * tn;
     p->threads = kThreads;
     return GEMM_OK;
@@ -239,7 +244,7 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
     kp.tiles_n = plan.tiles_n;
     kp.k_blocks = plan.k_steps;
     kp.raster_group = plan.raster_group;
-    kp.stages = plan.stages;
+    kp.slots = plan.slots;
     kp.release = plan.release;
     kp.wait_limit = cfg.wait_limit > 0 ? cfg.wait_limit : kDefaultWaitLimit;
     kp.inject = cfg.inject_stall;
@@ -296,7 +301,7 @@ const char* gemm_f16_strerror(int code) {
         case GEMM_ERR_DTYPE: return "out_dtype must be GEMM_OUT_F16 (0) or GEMM_OUT_F32 (1)";
         case GEMM_ERR_ALIGN: return "pointers must be 16-byte aligned and N, K multiples of 8";
         case GEMM_ERR_ALIAS: return "C overlaps A or B";
-        case GEMM_ERR_CONFIG: return "invalid tuning config (release must be < stages; tile_n 128 or 256)";
+        case GEMM_ERR_CONFIG: return "invalid tuning config (stages must exceed release; tile_n 128 or 256; ring must fit shared memory)";
         case GEMM_ERR_TMAP: return "the driver refused a TMA tensor-map encoding";
         case GEMM_ERR_LAUNCH: return "kernel launch failed";
         case GEMM_ERR_CUDA: return "no usable CUDA device or driver";

@@ -1,20 +1,21 @@
 // Persistent, warp-specialised fp16 GEMM for sm_103a: C[M,N] = A[M,K] * B[K,N],
 // fp32 accumulation in Tensor Memory, fp16 or fp32 output.
 //
-// Method ("JAX Pallas Mosaic GPU quickstart", "Hopper matrix multiplication
-// kernel" and "Key emit_pipeline parameters"; "Pallas software pipelining
-// guide", sections 3, 4 and 9.2):
+// Method ("Quickstart: GPU", section "Pipelining: a matmul kernel";
+// "JAX Pallas Mosaic GPU 快速上手", section "深入emit_pipeline的关键参数";
+// "JAX Pallas 软件流水线 Software Pipelining 完全指南", sections 3, 4 and 9.2):
 //   - a parallel grid of output tiles, each owned by exactly one block
 //     (here: a persistent CTA walks tile ids in a grouped raster order);
 //   - a sequential pipeline along K whose GMEM->SMEM copies overlap the
 //     tensor-core work through a multi-buffered shared-memory ring
-//     (max_concurrent_steps -> `stages`);
+//     (max_concurrent_steps -> `stages` loads in flight);
 //   - a buffer is reused only once the MMAs reading it have finished
-//     (delay_release -> tcgen05.commit onto the slot's `empty` barrier, plus
-//     an optional extra depth `release`);
+//     (tcgen05.commit onto the slot's `empty` barrier), plus an optional
+//     delay of `release` more steps (delay_release); the ring therefore has
+//     slots = stages + release buffers;
 //   - the fp32 accumulator (plgpu.ACC) lives in TMEM; the first K step of a
 //     tile overwrites it instead of adding (the zero-init rule of the
-//     pipelining guide's reduction example, section 7.2);
+//     software-pipelining guide's reduction example, section 7.2);
 //   - the drain converts the accumulator to the output type, stages it in
 //     shared memory, fences it for the async proxy and TMA-stores it.
 //
@@ -54,8 +55,8 @@ struct KernelParams {
     int M, N, K;
     int tiles_m, tiles_n, k_blocks;
     int raster_group;      // m-blocks per raster group
-    int stages;            // ring depth, 1 .. kMaxStages
-    int release;           // extra release depth, 0 .. stages-1
+    int slots;             // ring buffers = stages in flight + release depth, 1 .. kMaxStages
+    int release;           // extra release depth, 0 .. slots-1
     long long wait_limit;  // clock cycles a single wait may take before giving up
     int inject;            // test hook: 1 = the producer issues no loads at all
 };
@@ -71,7 +72,7 @@ struct Layout {
     static constexpr int kTmemCols = 2 * BN;             // two accumulators
     static constexpr int kNumBars = 2 * kMaxStages + 5;
     static constexpr int kFixedBytes = 4 * 2 * kStagingBytes + kNumBars * 8 + 16;
-    static constexpr int smem_bytes(int stages) { return stages * kStageBytes + kFixedBytes + 1024; }
+    static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
 };
 
 // Instruction descriptor, kind::f16: D fp32, A and B fp16, A K-major, B
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
-    const int S = p.stages;
+    const int S = p.slots;
     const uint32_t sA = base;
     const uint32_t sB = sA + S * L::kABytes;
     const uint32_t sC = sB + S * L::kBBytes;

@@ -5,7 +5,7 @@ arithmetic.  Both the CUDA path and the CPU oracle take their inputs from it,
 and it imports neither.
 
 The workloads are those of the matmul(a, b, out_dtype) statement of the
-"JAX Pallas Mosaic GPU quickstart" ("Hopper matrix multiplication kernel":
+"Quickstart: GPU" page ("Pipelining: a matmul kernel":
 fp16 operands, fp32 accumulator, fp16 or fp32 output), at five shapes:
 
   gemm_256     M=N=K=256,   A, B ~ U[-1, 1],            fp16 out

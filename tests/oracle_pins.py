@@ -11,7 +11,7 @@ The sources of truth, none of which is the oracle itself:
   - exact integer arithmetic on the scaled fp16 values (``exact.py``),
   - numpy's float64 matmul within the textbook summation bound,
   - closed forms: all-ones products, the identity, zero padding,
-  - the values the quickstart page prints for its fill_42 and iota kernels,
+  - the values "Quickstart: GPU" prints for its fill_42 and iota kernels,
     restated as products (``tests/golden``).
 """
 from __future__ import annotations

@@ -89,6 +89,7 @@ def test_plan_matches_the_tiling_arithmetic(lib):
         assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
         assert p["grid"] == min(p["num_tiles"], 152)
         assert 1 <= p["stages"] <= 8 and p["release"] < p["stages"]
+        assert p["slots"] == p["stages"] + p["release"]
         assert p["smem_bytes"] <= 232448
     # the 256^3 case is 2 x 2 tiles of 128 x 128 with 4 K steps
     p = tc.gemm_f16_plan(256, 256, 256, 0, num_sms=152)
@@ -107,19 +108,25 @@ def test_plan_ragged_and_degenerate(lib):
 
 
 def test_stages_clamp_and_release_rule(lib):
-    """The ring depth is clamped to the steps one CTA runs (emit_pipeline
-    clamps max_concurrent_steps to the grid) and must exceed the release
-    depth (emit_pipeline raises ValueError otherwise)."""
+    """`stages` is max_concurrent_steps and `release` is delay_release: the
+    ring holds stages + release buffers.  stages is clamped to the steps one
+    CTA runs and must exceed release, as emit_pipeline requires."""
     try:
         p = tc.gemm_f16_plan(128, 128, 128, 0, num_sms=152)  # 2 steps, 1 tile
-        assert p["stages"] == 2
+        assert (p["stages"], p["slots"]) == (2, 2)
         p = tc.gemm_f16_plan(128, 128, 64, 0, num_sms=152)   # 1 step
-        assert p["stages"] == 1
+        assert (p["stages"], p["slots"]) == (1, 1)
+        p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)
+        assert (p["tile_n"], p["stages"], p["release"], p["slots"]) == (256, 4, 0, 4)
+        # the pages' example: max_concurrent_steps=2, delay_release=1 -> 3 buffers
         tc.gemm_f16_set_config(stages=2, release=1)
         p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)
-        assert (p["stages"], p["release"]) == (2, 1)
+        assert (p["stages"], p["release"], p["slots"]) == (2, 1, 3)
         p = tc.gemm_f16_plan(128, 128, 64, 0, num_sms=152)   # clamp stops above release
-        assert p["stages"] == 2
+        assert (p["stages"], p["slots"]) == (2, 3)
+        tc.gemm_f16_set_config(release=1)                      # default stages: fill the ring
+        p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)
+        assert (p["stages"], p["release"], p["slots"]) == (3, 1, 4)
         with pytest.raises(tc.GemmError) as e:
             tc.gemm_f16_set_config(stages=2, release=2)
         assert e.value.code == CONFIG
@@ -127,8 +134,10 @@ def test_stages_clamp_and_release_rule(lib):
             tc.gemm_f16_set_config(tile_n=192)
         with pytest.raises(tc.GemmError):
             tc.gemm_f16_set_config(stages=9)
-        # a config the shared memory cannot hold is refused at plan time
-        tc.gemm_f16_set_config(tile_n=256, stages=8)
+        with pytest.raises(tc.GemmError):
+            tc.gemm_f16_set_config(stages=6, release=3)
+        # a ring the shared memory cannot hold is refused at plan time
+        tc.gemm_f16_set_config(tile_n=256, stages=4, release=1)
         with pytest.raises(tc.GemmError) as e:
             tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)
         assert e.value.code == CONFIG

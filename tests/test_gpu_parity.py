@@ -73,8 +73,10 @@ def test_ragged_shapes(M, N, K, out_dtype):
     check_full(a, b, out_dtype, f"ragged {M}x{N}x{K}")
 
 
+# every ring the shared memory holds: 6 buffers at tile_n 128, 4 at 256
 VARIANTS = [dict(tile_n=t, stages=s, release=r)
-            for t in (128, 256) for s in (1, 2, 3, 4) for r in (0, 1, 2) if r < s]
+            for t in (128, 256) for s in (1, 2, 3, 4, 5, 6) for r in (0, 1, 2)
+            if r < s and s + r <= (6 if t == 128 else 4)]
 
 
 @pytest.mark.parametrize("cfg", VARIANTS, ids=lambda c: f"n{c['tile_n']}s{c['stages']}r{c['release']}")
