@@ -299,7 +299,7 @@ def workload_config(w, plan) -> dict:
            "inputs": f"A ~ {w.a_dist[0]}({w.a_dist[1]:g}), B ~ {w.b_dist[0]}({w.b_dist[1]:g}), fp16, seeds 0/1",
            "l2": "inputs rotated over 3 copies, each larger than L2 (A+B+C > 126 MB)"}
     if plan is not None:
-        cfg["plan"] = {k: plan[k] for k in ("tile_m", "tile_n", "tile_k", "stages", "release", "slots", "grid",
+        cfg["plan"] = {k: plan[k] for k in ("tile_m", "tile_n", "tile_k", "stages", "release", "slots", "split", "grid",
                                             "raster_group", "num_tiles", "k_steps")}
     return cfg
 

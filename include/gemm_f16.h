@@ -70,7 +70,8 @@ typedef struct {
     int stages;                 /* loads in flight ahead of the MMA (max_concurrent_steps) */
     int release;                /* extra steps before a buffer is reused (delay_release) */
     int slots;                  /* shared-memory ring buffers: stages + release */
-    int grid;                   /* persistent CTAs launched */
+    int split;                  /* CTAs (one thread-block cluster) sharing each tile along K */
+    int grid;                   /* CTAs launched: persistent, or num_tiles * split with split-K */
     int raster_group;           /* m-blocks per raster group */
     int smem_bytes;             /* dynamic shared memory per CTA */
     int tmem_cols;              /* Tensor Memory columns per CTA */
@@ -86,6 +87,7 @@ typedef struct {
     int grid;              /* 0 = min(num_tiles, SM count); else a cap on the CTAs launched */
     int raster_group;      /* 0 or >= 1 */
     long long wait_limit;  /* 0 = about one second; else clock cycles one device wait may take */
+    int split;             /* 0 = planner default; 1 = no split-K; 2..8 = CTAs per tile along K */
     int inject_stall;      /* test hook: 1 makes every CTA's producer issue no loads, so
                               the MMA warp's bounded wait runs out and the kernel reports
                               GEMM_ERR_DEVICE_TIMEOUT instead of finishing.  0 in normal use. */
@@ -141,7 +143,8 @@ const char *gemm_f16_strerror(int code);
  * library gave up on a bounded wait since the last reset: GEMM_OK or
  * GEMM_ERR_DEVICE_TIMEOUT.  *site (if not NULL) receives which wait gave up
  * first (1 producer/empty slot, 2 MMA/full slot, 3 MMA/free accumulator,
- * 4 epilogue/ready accumulator, 5 drain), 0 if none.  reset != 0 clears it.
+ * 4 epilogue/ready accumulator, 5 drain, 6 split-K partials ready, 7 split-K
+ * partials read), 0 if none.  reset != 0 clears it.
  */
 int gemm_f16_device_status(int *site, int reset);
 

@@ -69,6 +69,7 @@ int check_config(const gemm_config& c) {
     if (c.stages + c.release > kMaxStages) return GEMM_ERR_CONFIG;
     if (c.grid < 0 || c.raster_group < 0 || c.wait_limit < 0) return GEMM_ERR_CONFIG;
     if (c.inject_stall != 0 && c.inject_stall != 1) return GEMM_ERR_CONFIG;
+    if (c.split < 0 || c.split > kMaxSplit) return GEMM_ERR_CONFIG;
     return GEMM_OK;
 }
 
@@ -84,8 +85,13 @@ int max_slots_for(int tile_n, int out_dtype) {
     return s;
 }
 
-// The planner.  Tile: 128 x 256 when there are at least as many such tiles as
-// SMs, else 128 x 128 (more tiles for small or skinny problems).
+// The planner.
+// Tile: 128 x 256 or 128 x 128, whichever needs less time counted in waves of
+// tiles over the SMs, a 128 x 128 tile costing 0.6 of a 128 x 256 one (half
+// the MMA work at a lower tensor-pipe efficiency: it needs the whole
+// shared-memory port per SM).
+// Split-K: when the tiles fill less than half the SMs, a cluster of `split`
+// CTAs shares each tile along K (at least 16 K steps each), one tile per cluster.
 // Pipeline depth, in the pages' terms: `stages` (max_concurrent_steps) loads in
 // flight ahead of the MMA and `release` (delay_release) extra steps before a
 // buffer is handed back, so the ring holds stages + release buffers.  As in
@@ -96,30 +102,58 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
     std::memset(p, 0, sizeof(*p));
     p->tile_m = kBM;
     p->tile_k = kBK;
+    const int tiles_m = ceil_div(M, kBM);
     int tn = cfg.tile_n;
     if (tn == 0) {
-        const long long tiles256 = (long long)ceil_div(M, kBM) * ceil_div(N, 256);
-        tn = tiles256 >= num_sms ? 256 : 128;
+        const long long w256 = ((long long)tiles_m * ceil_div(N, 256) + num_sms - 1) / num_sms;
+        const long long w128 = ((long long)tiles_m * ceil_div(N, 128) + num_sms - 1) / num_sms;
+        tn = w256 * 10 <= w128 * 6 ? 256 : 128;
     }
     p->tile_n = tn;
-    p->tiles_m = ceil_div(M, kBM);
+    p->tiles_m = tiles_m;
     p->tiles_n = ceil_div(N, tn);
     p->num_tiles = p->tiles_m * p->tiles_n;
     p->k_steps = ceil_div(K, kBK);
-    p->grid = p->num_tiles < num_sms ? p->num_tiles : num_sms;
-    if (cfg.grid > 0 && cfg.grid < p->grid) p->grid = cfg.grid;
+
+    int split = cfg.split;
+    if (split == 0) {
+        split = 1;
+        if (p->num_tiles > 0 && 2 * p->num_tiles <= num_sms) {
+            split = num_sms / p->num_tiles;
+            if (split > kMaxSplit) split = kMaxSplit;
+            if (split > p->k_steps / 16) split = p->k_steps / 16;
+            if (split < 1) split = 1;
+        }
+    }
+    if (split > 1 && split > p->k_steps) return GEMM_ERR_CONFIG;
+    p->split = split;
+    if (split > 1) {
+        p->grid = p->num_tiles * split;  // one tile per cluster
+    } else {
+        p->grid = p->num_tiles < num_sms ? p->num_tiles : num_sms;
+        if (cfg.grid > 0 && cfg.grid < p->grid) p->grid = cfg.grid;
+    }
     if (p->grid < 1) p->grid = 1;
+
     const int d = cfg.release;
     const int max_slots = max_slots_for(tn, out_dtype);
     int s = cfg.stages > 0 ? cfg.stages : max_slots - d;
     if (s <= d) return GEMM_ERR_CONFIG;
     if (s + d > max_slots) return GEMM_ERR_CONFIG;
-    const long long steps_per_cta = (long long)p->k_steps * ceil_div(p->num_tiles, p->grid);
+    const long long ctas_per_tile_slot = split > 1 ? 1 : ceil_div(p->num_tiles, p->grid);
+    const long long steps_per_cta = (long long)ceil_div(p->k_steps, split) * ctas_per_tile_slot;
     if (steps_per_cta < s) s = (int)(steps_per_cta > d ? steps_per_cta : d + 1);
+    if (split > 1) {
+        // the other ranks park an fp32 partial tile in their ring buffers
+        const int stage_bytes = kBM * kBK * 2 + kBK * tn * 2;
+        const int need = (kBM * tn * 4 + stage_bytes - 1) / stage_bytes;
+        if (s + d < need) s = need - d;
+        if (s + d > max_slots) return GEMM_ERR_CONFIG;
+    }
     p->stages = s;
     p->release = d;
     p->slots = s + d;
-    p->raster_group = cfg.raster_group > 0 ? cfg.raster_group : 8;
+    p->raster_group = cfg.raster_group > 0 ? cfg.raster_group : 16;
     p->smem_bytes = smem_for(tn, out_dtype, p->slots);
     p->tmem_cols = 2 * tn;
     p->threads = kThreads;
@@ -176,19 +210,28 @@ template <int BN, int OUT>
 int launch(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
            const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
     auto kern = gemm_f16_kernel<BN, OUT>;
-    bool& attr = dev.attr_set[BN == 256][OUT];
-    if (!attr) {
+    bool& attr_done = dev.attr_set[BN == 256][OUT];
+    if (!attr_done) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_LAUNCH;
         }
-        attr = true;
+        attr_done = true;
     }
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(plan.grid, 1, 1);
     lc.blockDim = dim3(kThreads, 1, 1);
     lc.dynamicSmemBytes = plan.smem_bytes;
     lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (plan.split > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = plan.split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+    }
     cudaError_t e = cudaLaunchKernelEx(&lc, kern, ta, tb, tc, kp);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -246,6 +289,7 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
     kp.raster_group = plan.raster_group;
     kp.slots = plan.slots;
     kp.release = plan.release;
+    kp.split = plan.split;
     kp.wait_limit = cfg.wait_limit > 0 ? cfg.wait_limit : kDefaultWaitLimit;
     kp.inject = cfg.inject_stall;
 

@@ -19,6 +19,15 @@
 //   - the drain converts the accumulator to the output type, stages it in
 //     shared memory, fences it for the async proxy and TMA-stores it.
 //
+// Split-K (split > 1): a cluster of `split` CTAs owns one tile; CTA rank r
+// runs its own contiguous share of the K steps into its own TMEM, and the
+// partial sums meet in the rank-0 CTA through distributed shared memory:
+// every other rank parks its fp32 partial in its (now idle) ring buffers and
+// arrives on rank 0's `red_ready` barrier; rank 0 adds them in rank order
+// (deterministic), drains the tile as above and arrives on each rank's
+// `red_done`, which keeps that rank's shared memory alive until it is read.
+// The planner gives each cluster exactly one tile in this mode.
+//
 // Roles (192 threads, one CTA per SM):
 //   warp 0       TMA producer (one lane)
 //   warp 1       MMA issuer (one lane); allocates/frees TMEM (whole warp)
@@ -37,6 +46,7 @@ constexpr int kBK = 64;        // K per pipeline step: one 128-byte swizzle row 
 constexpr int kUmmaK = 16;     // K of one tcgen05.mma with 16-bit operands
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kMaxStages = 8;
+constexpr int kMaxSplit = 8;   // portable cluster size
 constexpr int kBoxBytes = kBK * 64 * 2;  // one 64 x 64 fp16 box of B: 8 KiB
 
 // Status word written by a CTA whose bounded wait ran out (first writer wins).
@@ -47,6 +57,8 @@ enum WaitSite : unsigned {
     kSiteMmaTmemEmpty = 3,
     kSiteEpilogueTmemFull = 4,
     kSiteDrain = 5,
+    kSiteReduceReady = 6,
+    kSiteReduceDone = 7,
 };
 
 __device__ unsigned int g_status;
@@ -57,6 +69,7 @@ struct KernelParams {
     int raster_group;      // m-blocks per raster group
     int slots;             // ring buffers = stages in flight + release depth, 1 .. kMaxStages
     int release;           // extra release depth, 0 .. slots-1
+    int split;             // CTAs (one cluster) sharing a tile along K; 1 = no split
     long long wait_limit;  // clock cycles a single wait may take before giving up
     int inject;            // test hook: 1 = the producer issues no loads at all
 };
@@ -70,7 +83,9 @@ struct Layout {
     static constexpr int kOutCols = OUT == 0 ? 64 : 32;  // columns in one 128-byte output row
     static constexpr int kStagingBytes = 32 * 128;       // one warp's 32 rows x 128 bytes
     static constexpr int kTmemCols = 2 * BN;             // two accumulators
-    static constexpr int kNumBars = 2 * kMaxStages + 5;
+    static constexpr int kPartialBytes = kBM * BN * 4;   // one fp32 partial tile (split-K)
+    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain, red_ready, red_done
+    static constexpr int kNumBars = 2 * kMaxStages + 7;
     static constexpr int kFixedBytes = 4 * 2 * kStagingBytes + kNumBars * 8 + 16;
     static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
 };
@@ -110,11 +125,17 @@ __device__ __forceinline__ void record_timeout(unsigned site) { atomicCAS(&g_sta
 
 // Bounded wait on an mbarrier phase.  Gives up (returning false) when the
 // CTA-wide abort flag is raised or, after `limit` cycles, raises it itself.
+// kClusterAcquire: acquire at cluster scope (the data was written by another
+// CTA of the cluster before it arrived).
+template <bool kClusterAcquire = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              long long limit, unsigned site) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto probe = [&]() {
+        return kClusterAcquire ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (probe()) return true;
     const long long t0 = clock64();
-    while (!ptx::mbar_try_wait(bar, parity)) {
+    while (!probe()) {
         if (*abort_flag) return false;
         if (clock64() - t0 > limit) {
             *abort_flag = 1;
@@ -138,11 +159,62 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, long l
     return true;
 }
 
+// Lane 0 waits, the warp follows its verdict.
+template <bool kClusterAcquire = false>
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long limit,
+                                          unsigned site, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bounded<kClusterAcquire>(bar, parity, abort_flag, limit, site);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// One 128-byte-wide column chunk of a warp's 32 output rows: convert, write
+// to the warp's staging buffer in the 128-byte swizzle the C tensor map
+// expects (16-byte chunk j of row `lane` at chunk j ^ (lane % 8)), fence for
+// the async proxy and TMA-store it.  Staging is double-buffered per warp.
+template <int OUT>
+__device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 32], const CUtensorMap* tmC,
+                                            uint32_t staging, int& nstore, int lane, int x, int y) {
+    const uint32_t stg = staging + (uint32_t)((nstore & 1) * 4096);
+    // the store issued from this buffer two rounds ago must have read it
+    if (lane == 0) ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+    const uint32_t row_addr = stg + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w0, w1, w2, w3;
+        if constexpr (OUT == 0) {
+            w0 = ptx::pack_f16x2(v[8 * j + 0], v[8 * j + 1]);
+            w1 = ptx::pack_f16x2(v[8 * j + 2], v[8 * j + 3]);
+            w2 = ptx::pack_f16x2(v[8 * j + 4], v[8 * j + 5]);
+            w3 = ptx::pack_f16x2(v[8 * j + 6], v[8 * j + 7]);
+        } else {
+            w0 = v[4 * j + 0];
+            w1 = v[4 * j + 1];
+            w2 = v[4 * j + 2];
+            w3 = v[4 * j + 3];
+        }
+        ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        ptx::tma_store_2d(tmC, stg, x, y);
+        ptx::bulk_commit_group();
+    }
+    ++nstore;
+}
+
+__device__ __forceinline__ void fadd_bits(uint32_t& acc, uint32_t add) {
+    acc = __float_as_uint(__uint_as_float(acc) + __uint_as_float(add));
+}
+
 template <int BN, int OUT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
     using L = Layout<BN, OUT>;
+    constexpr int kCols = L::kOutCols;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must sit on 1024-byte boundaries
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -162,9 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kMaxStages + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kMaxStages + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+    const uint32_t red_ready_bar = bar0 + 8u * (2 * kMaxStages + 5);
+    const uint32_t red_done_bar = bar0 + 8u * (2 * kMaxStages + 6);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int split = p.split;
+    const uint32_t rank = split > 1 ? ptx::cluster_ctarank() : 0u;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -176,6 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(tempty_bar(a), 4);  // one arrive per epilogue warp
         }
         ptx::mbar_init(drain_bar, 1);
+        // split-K: each other rank's 4 epilogue warps arrive on rank 0's red_ready,
+        // rank 0's 4 epilogue warps on every other rank's red_done
+        ptx::mbar_init(red_ready_bar, split > 1 ? 4 * (split - 1) : 1);
+        ptx::mbar_init(red_done_bar, 4);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -190,11 +270,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
+    // every CTA of the cluster has its barriers initialised before any remote arrive
+    if (split > 1) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const int num_tiles = p.tiles_m * p.tiles_n;
-    const int KB = p.k_blocks;
+    const int first_tile = blockIdx.x / split;
+    const int tile_stride = gridDim.x / split;
+    // this CTA's share of the K steps (all of them without split-K)
+    const int kb_begin = (int)((long long)p.k_blocks * rank / split);
+    const int kb_end = (int)((long long)p.k_blocks * (rank + 1) / split);
+    const int KB = kb_end - kb_begin;
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -205,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;  // per slot: ever issued, parity of last issue
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            for (int t = first_tile; ok && t < num_tiles; t += tile_stride) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -242,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long it = 0;
             int tl = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x, ++tl) {
+            for (int t = first_tile; ok && t < num_tiles; t += tile_stride, ++tl) {
                 const int acc = tl & 1;
                 const uint32_t aph = (tl >> 1) & 1;
                 if (!wait_bounded(tempty_bar(acc), aph ^ 1u, abort_flag, p.wait_limit, kSiteMmaTmemEmpty)) {
@@ -290,35 +377,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ---------------- epilogue: TMEM -> registers -> SMEM -> TMA store ----------------
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const uint32_t staging = sC + (uint32_t)(q * 2 * L::kStagingBytes);
+        const int row_in_tile = q * 32 + lane;
         int tl = 0;
         int nstore = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tl) {
+        for (int t = first_tile; t < num_tiles; t += tile_stride, ++tl) {
             int mb, nb;
             tile_coords(t, p, mb, nb);
             const int acc = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
             if (KB > 0) {
-                int ok = 1;
                 // a legitimate wait here spans a whole tile's main loop: allow 4x
-                if (lane == 0)
-                    ok = wait_bounded(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
+                if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane))
+                    break;
                 ptx::tc_fence_after();
             }
             const int row0 = mb * kBM + q * 32;
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            constexpr int kChunks = BN / L::kOutCols;
+
+            if (split > 1 && rank != 0) {
+                // park this rank's fp32 partial in its idle ring buffers, laid out as
+                // [column / 4][row] 16-byte groups so consecutive lanes touch
+                // consecutive 16 bytes (no bank conflicts, here or in rank 0's reads)
 #pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                uint32_t v[L::kOutCols];
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    if (KB > 0) {
+                        ptx::tmem_ld_32x32b_x32(trow + c * 32, v);
+                        ptx::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        ptx::st_shared_v4(sA + (uint32_t)(((c * 8 + j) * kBM + row_in_tile) * 16), v[4 * j],
+                                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, 0));
+                // rank 0 reads this shared memory; stay until it says it is done
+                warp_wait(red_done_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceDone, lane);
+                continue;
+            }
+            if (split > 1) {
+                if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane)) break;
+            }
+
+#pragma unroll 1
+            for (int c = 0; c < BN / kCols; ++c) {
+                uint32_t v[kCols];
                 if (KB > 0) {
-                    ptx::tmem_ld_32x32b_x32(trow + c * L::kOutCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                    ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                     if constexpr (OUT == 0)
-                        ptx::tmem_ld_32x32b_x32(trow + c * L::kOutCols + 32,
-                                                *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                        ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                     ptx::tmem_ld_wait();
-                    if (c == kChunks - 1) {
+                    if (c == BN / kCols - 1) {
                         // accumulator fully read: hand it back to the MMA warp
                         ptx::tc_fence_before();
                         __syncwarp();
@@ -326,38 +440,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < L::kOutCols; ++i) v[i] = 0u;  // empty sum (K = 0)
+                    for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
                 }
-                const uint32_t stg = sC + (uint32_t)((q * 2 + (nstore & 1)) * L::kStagingBytes);
-                // the store issued from this buffer two rounds ago must have read it
-                if (lane == 0) ptx::bulk_wait_group_read<1>();
-                __syncwarp();
-                const uint32_t row_addr = stg + lane * 128;
+                // split-K: add the other ranks' partials, in rank order
+                for (int r = 1; r < split; ++r) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t w0, w1, w2, w3;
-                    if constexpr (OUT == 0) {
-                        w0 = ptx::pack_f16x2(v[8 * j + 0], v[8 * j + 1]);
-                        w1 = ptx::pack_f16x2(v[8 * j + 2], v[8 * j + 3]);
-                        w2 = ptx::pack_f16x2(v[8 * j + 4], v[8 * j + 5]);
-                        w3 = ptx::pack_f16x2(v[8 * j + 6], v[8 * j + 7]);
-                    } else {
-                        w0 = v[4 * j + 0];
-                        w1 = v[4 * j + 1];
-                        w2 = v[4 * j + 2];
-                        w3 = v[4 * j + 3];
+                    for (int j = 0; j < kCols / 4; ++j) {
+                        const int g = c * (kCols / 4) + j;  // 16-byte column group
+                        const uint32_t addr = ptx::mapa(sA + (uint32_t)((g * kBM + row_in_tile) * 16), (uint32_t)r);
+                        uint32_t x0, x1, x2, x3;
+                        ptx::ld_cluster_v4(addr, x0, x1, x2, x3);
+                        fadd_bits(v[4 * j], x0);
+                        fadd_bits(v[4 * j + 1], x1);
+                        fadd_bits(v[4 * j + 2], x2);
+                        fadd_bits(v[4 * j + 3], x3);
                     }
-                    // 16-byte chunk j of row `lane` goes to chunk j ^ (lane % 8): the
-                    // 128-byte swizzle the C tensor map expects
-                    ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
                 }
-                ptx::fence_proxy_async_smem();
+                store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, row0);
+            }
+            if (split > 1) {
+                // every other rank's partial has been read
                 __syncwarp();
-                if (lane == 0) {
-                    ptx::tma_store_2d(&tmC, stg, nb * BN + c * L::kOutCols, row0);
-                    ptx::bulk_commit_group();
-                }
-                ++nstore;
+                if (lane == 0)
+                    for (int r = 1; r < split; ++r) ptx::mbar_arrive_cluster(ptx::mapa(red_done_bar, (uint32_t)r));
             }
         }
         if (lane == 0) ptx::bulk_wait_group<0>();

@@ -87,7 +87,10 @@ def test_plan_matches_the_tiling_arithmetic(lib):
         assert p["tile_m"] == 128 and p["tile_k"] == 64
         assert p["tiles_m"] == -(-w.M // 128) and p["tiles_n"] == -(-w.N // p["tile_n"])
         assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
-        assert p["grid"] == min(p["num_tiles"], 152)
+        if p["split"] == 1:
+            assert p["grid"] == min(p["num_tiles"], 152)
+        else:  # one tile per cluster of `split` CTAs
+            assert p["grid"] == p["num_tiles"] * p["split"] <= 152
         assert 1 <= p["stages"] <= 8 and p["release"] < p["stages"]
         assert p["slots"] == p["stages"] + p["release"]
         assert p["smem_bytes"] <= 232448
@@ -96,6 +99,41 @@ def test_plan_matches_the_tiling_arithmetic(lib):
     assert (p["tiles_m"], p["tiles_n"], p["tile_n"], p["k_steps"]) == (2, 2, 128, 4)
     # the big square problem takes the wide tile
     assert tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152)["tile_n"] == 256
+    # long K: 128 wide tiles in one wave beat 256 narrow ones in two
+    p = tc.gemm_f16_plan(2048, 2048, 32768, 1, num_sms=152)
+    assert (p["tile_n"], p["num_tiles"], p["split"], p["grid"]) == (256, 128, 1, 128)
+    # skinny: 64 narrow tiles would fill under half the SMs, so two CTAs share each along K
+    p = tc.gemm_f16_plan(128, 8192, 8192, 0, num_sms=152)
+    assert (p["tile_n"], p["num_tiles"], p["split"], p["grid"]) == (128, 64, 2, 128)
+
+
+def test_split_k_planning(lib):
+    try:
+        # few tiles, long K: as many CTAs per tile as fit, at most 8, >= 16 steps each
+        p = tc.gemm_f16_plan(128, 128, 65536, 0, num_sms=152)
+        assert (p["split"], p["grid"]) == (8, 8)
+        p = tc.gemm_f16_plan(128, 128, 1024, 0, num_sms=152)   # 16 K steps: no split
+        assert p["split"] == 1
+        p = tc.gemm_f16_plan(128, 128, 2048, 0, num_sms=152)   # 32 K steps: 2 CTAs
+        assert p["split"] == 2
+        # the other ranks' fp32 partial must fit their ring: 64 KiB at tile_n 128,
+        # 128 KiB at tile_n 256 (three 48 KiB buffers)
+        tc.gemm_f16_set_config(split=2, stages=1)
+        p = tc.gemm_f16_plan(128, 1024, 8192, 0, num_sms=152)
+        assert p["slots"] * (16384 + 128 * p["tile_n"]) >= 128 * p["tile_n"] * 4
+        tc.gemm_f16_set_config(split=4, tile_n=256)
+        p = tc.gemm_f16_plan(256, 512, 4096, 1, num_sms=152)
+        assert (p["split"], p["grid"]) == (4, 16) and p["slots"] >= 3
+        tc.gemm_f16_set_config(split=4)
+        with pytest.raises(tc.GemmError) as e:                  # fewer K steps than CTAs
+            tc.gemm_f16_plan(128, 128, 192, 0, num_sms=152)
+        assert e.value.code == CONFIG
+        with pytest.raises(tc.GemmError):
+            tc.gemm_f16_set_config(split=9)
+        tc.gemm_f16_set_config(split=1)
+        assert tc.gemm_f16_plan(128, 8192, 8192, 0, num_sms=152)["split"] == 1
+    finally:
+        tc.gemm_f16_set_config()
 
 
 def test_plan_ragged_and_degenerate(lib):

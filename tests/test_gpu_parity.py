@@ -97,6 +97,26 @@ def test_persistent_many_tiles_per_cta(tile_n):
     check_full(a, b, 0, f"persistent tile_n={tile_n}")
 
 
+SPLITS = [(2, 128, 0), (2, 256, 1), (3, 128, 0), (4, 128, 1), (8, 128, 0), (5, 256, 0)]
+
+
+@pytest.mark.parametrize("split,tile_n,out_dtype", SPLITS)
+def test_split_k(split, tile_n, out_dtype):
+    """Split-K through a cluster: K steps shared unevenly (47 steps), ragged
+    M, N and K, partials summed in rank 0 through distributed shared memory."""
+    tc.gemm_f16_set_config(split=split, tile_n=tile_n)
+    a, b = make_inputs(200, 520, 2984, ("normal", 1.0), ("normal", 1.0), seed_a=split, seed_b=tile_n)
+    check_full(a, b, out_dtype, f"split {split} tile_n {tile_n}")
+
+
+def test_split_k_is_deterministic():
+    tc.gemm_f16_set_config(split=4)
+    a, b = make_inputs(128, 1024, 4096, ("uniform", 1.0), ("uniform", 1.0), seed_a=1, seed_b=2)
+    c1 = gpu_gemm(a, b, 1)
+    c2 = gpu_gemm(a, b, 1)
+    assert torch.equal(c1.view(torch.int32), c2.view(torch.int32))
+
+
 def test_subnormal_and_scaled_inputs():
     # N(0,1)/64 inputs put ~0.3% of entries in the fp16 subnormal range
     a = draw((384, 512), ("normal", 1 / 64), 3)
