@@ -80,7 +80,7 @@ typedef struct {
 
 /* Tuning override.  Zero in a field means "planner default". */
 typedef struct {
-    int tile_n;            /* 0, 128 or 256 */
+    int tile_n;            /* 0, 64, 128 or 256 */
     int stages;            /* 0 or 1..8: loads in flight (max_concurrent_steps) */
     int release;           /* 0..7: delay_release; stages must exceed it, and
                               stages + release buffers must fit shared memory */

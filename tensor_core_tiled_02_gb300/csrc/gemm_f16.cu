@@ -27,7 +27,7 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int cc = 0;
-    bool attr_set[2][2] = {{false, false}, {false, false}};  // [tile_n == 256][out_dtype]
+    bool attr_set[3][2] = {};  // [tile_n 64 / 128 / 256][out_dtype]
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -62,7 +62,7 @@ int check_args(const void* A, const void* B, const void* C, int M, int N, int K,
 }
 
 int check_config(const gemm_config& c) {
-    if (c.tile_n != 0 && c.tile_n != 128 && c.tile_n != 256) return GEMM_ERR_CONFIG;
+    if (c.tile_n != 0 && c.tile_n != 64 && c.tile_n != 128 && c.tile_n != 256) return GEMM_ERR_CONFIG;
     if (c.stages < 0 || c.stages > kMaxStages) return GEMM_ERR_CONFIG;
     if (c.release < 0 || c.release >= kMaxStages) return GEMM_ERR_CONFIG;
     if (c.stages != 0 && c.release >= c.stages) return GEMM_ERR_CONFIG;
@@ -76,6 +76,8 @@ int check_config(const gemm_config& c) {
 int smem_for(int tile_n, int out_dtype, int slots) {
     if (tile_n == 256)
         return out_dtype == GEMM_OUT_F16 ? Layout<256, 0>::smem_bytes(slots) : Layout<256, 1>::smem_bytes(slots);
+    if (tile_n == 64)
+        return out_dtype == GEMM_OUT_F16 ? Layout<64, 0>::smem_bytes(slots) : Layout<64, 1>::smem_bytes(slots);
     return out_dtype == GEMM_OUT_F16 ? Layout<128, 0>::smem_bytes(slots) : Layout<128, 1>::smem_bytes(slots);
 }
 
@@ -87,9 +89,9 @@ int max_slots_for(int tile_n, int out_dtype) {
 
 // The planner.
 // Tile: 128 x 256 or 128 x 128, whichever needs less time counted in waves of
-// tiles over the SMs, a 128 x 128 tile costing 0.6 of a 128 x 256 one (half
-// the MMA work at a lower tensor-pipe efficiency: it needs the whole
-// shared-memory port per SM).
+// tiles over the SMs, a 128 x 128 tile costing 0.85 of a 128 x 256 one (half
+// the MMA work at about 0.6 of the tensor-pipe efficiency, measured: it needs
+// the whole shared-memory port per SM).  128 x 64 is only taken on request.
 // Split-K: when the tiles fill less than half the SMs, a cluster of `split`
 // CTAs shares each tile along K (at least 16 K steps each), one tile per cluster.
 // Pipeline depth, in the pages' terms: `stages` (max_concurrent_steps) loads in
@@ -107,7 +109,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
     if (tn == 0) {
         const long long w256 = ((long long)tiles_m * ceil_div(N, 256) + num_sms - 1) / num_sms;
         const long long w128 = ((long long)tiles_m * ceil_div(N, 128) + num_sms - 1) / num_sms;
-        tn = w256 * 10 <= w128 * 6 ? 256 : 128;
+        tn = w256 * 100 <= w128 * 85 ? 256 : 128;
     }
     p->tile_n = tn;
     p->tiles_m = tiles_m;
@@ -210,7 +212,7 @@ template <int BN, int OUT>
 int launch(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
            const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
     auto kern = gemm_f16_kernel<BN, OUT>;
-    bool& attr_done = dev.attr_set[BN == 256][OUT];
+    bool& attr_done = dev.attr_set[BN == 64 ? 0 : BN == 128 ? 1 : 2][OUT];
     if (!attr_done) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess) {
             cudaGetLastError();
@@ -223,15 +225,23 @@ int launch(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, 
     lc.blockDim = dim3(kThreads, 1, 1);
     lc.dynamicSmemBytes = plan.smem_bytes;
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    // programmatic serialisation: this kernel's prologue may overlap the tail
+    // of the previous kernel in the stream (it waits for that kernel's
+    // completion before touching global memory)
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     if (plan.split > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = plan.split;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        lc.attrs = attr;
-        lc.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = plan.split;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    lc.attrs = attr;
+    lc.numAttrs = na;
     cudaError_t e = cudaLaunchKernelEx(&lc, kern, ta, tb, tc, kp);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -297,6 +307,9 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
     if (plan.tile_n == 256)
         return out_dtype == GEMM_OUT_F16 ? launch<256, 0>(plan, ta, tb, tc, kp, s, *dev)
                                          : launch<256, 1>(plan, ta, tb, tc, kp, s, *dev);
+    if (plan.tile_n == 64)
+        return out_dtype == GEMM_OUT_F16 ? launch<64, 0>(plan, ta, tb, tc, kp, s, *dev)
+                                         : launch<64, 1>(plan, ta, tb, tc, kp, s, *dev);
     return out_dtype == GEMM_OUT_F16 ? launch<128, 0>(plan, ta, tb, tc, kp, s, *dev)
                                      : launch<128, 1>(plan, ta, tb, tc, kp, s, *dev);
 }

@@ -21,12 +21,18 @@
 //
 // Split-K (split > 1): a cluster of `split` CTAs owns one tile; CTA rank r
 // runs its own contiguous share of the K steps into its own TMEM, and the
-// partial sums meet in the rank-0 CTA through distributed shared memory:
-// every other rank parks its fp32 partial in its (now idle) ring buffers and
-// arrives on rank 0's `red_ready` barrier; rank 0 adds them in rank order
-// (deterministic), drains the tile as above and arrives on each rank's
-// `red_done`, which keeps that rank's shared memory alive until it is read.
+// partial sums meet through distributed shared memory.  The tile's output
+// column chunks are dealt out round-robin (chunk c belongs to rank c % split).
+// Every rank parks its fp32 partial of the chunks it does not own in its (now
+// idle) ring buffers and arrives on the other ranks' `red_ready` barriers;
+// each rank then adds, for the chunks it owns, the other ranks' partials to
+// its own in ascending rank order (deterministic), drains them as above, and arrives on the others'
+// `red_done`, which keeps every rank's shared memory alive until it is read.
 // The planner gives each cluster exactly one tile in this mode.
+//
+// Programmatic dependent launch: the prologue (barriers, TMEM, tensor-map
+// prefetch) runs before `griddepcontrol.wait`, so it overlaps the tail of the
+// previous kernel in the stream; no global memory is touched before the wait.
 //
 // Roles (192 threads, one CTA per SM):
 //   warp 0       TMA producer (one lane)
@@ -76,7 +82,7 @@ struct KernelParams {
 
 template <int BN, int OUT>
 struct Layout {
-    static_assert(BN == 128 || BN == 256, "tile N");
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile N");
     static constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
     static constexpr int kBBytes = kBK * BN * 2;   // BN/64 boxes of 8 KiB
     static constexpr int kStageBytes = kABytes + kBBytes;
@@ -252,10 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(tempty_bar(a), 4);  // one arrive per epilogue warp
         }
         ptx::mbar_init(drain_bar, 1);
-        // split-K: each other rank's 4 epilogue warps arrive on rank 0's red_ready,
-        // rank 0's 4 epilogue warps on every other rank's red_done
+        // split-K: the 4 epilogue warps of every other rank arrive on these
         ptx::mbar_init(red_ready_bar, split > 1 ? 4 * (split - 1) : 1);
-        ptx::mbar_init(red_done_bar, 4);
+        ptx::mbar_init(red_done_bar, split > 1 ? 4 * (split - 1) : 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -274,6 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (split > 1) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the previous kernel's writes (and reads) of A, B and C are done from here on
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
 
     const int num_tiles = p.tiles_m * p.tiles_n;
     const int first_tile = blockIdx.x / split;
@@ -395,44 +403,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = mb * kBM + q * 32;
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 
-            if (split > 1 && rank != 0) {
-                // park this rank's fp32 partial in its idle ring buffers, laid out as
+            if (split > 1) {
+                // park the partial of every chunk another rank owns, laid out as
                 // [column / 4][row] 16-byte groups so consecutive lanes touch
-                // consecutive 16 bytes (no bank conflicts, here or in rank 0's reads)
+                // consecutive 16 bytes (no bank conflicts, here or in the remote reads)
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
-                    if (KB > 0) {
-                        ptx::tmem_ld_32x32b_x32(trow + c * 32, v);
-                        ptx::tmem_ld_wait();
-                    } else {
+                for (int c = 0; c < BN / kCols; ++c) {
+                    if (c % split == (int)rank) continue;
+#pragma unroll 1
+                    for (int h = 0; h < kCols / 32; ++h) {
+                        uint32_t v[32];
+                        const int col = c * kCols + h * 32;
+                        if (KB > 0) {
+                            ptx::tmem_ld_32x32b_x32(trow + col, v);
+                            ptx::tmem_ld_wait();
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0u;
+                            for (int i = 0; i < 32; ++i) v[i] = 0u;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            ptx::st_shared_v4(sA + (uint32_t)(((col / 4 + j) * kBM + row_in_tile) * 16), v[4 * j],
+                                              v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        ptx::st_shared_v4(sA + (uint32_t)(((c * 8 + j) * kBM + row_in_tile) * 16), v[4 * j],
-                                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, 0));
-                // rank 0 reads this shared memory; stay until it says it is done
-                warp_wait(red_done_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceDone, lane);
-                continue;
-            }
-            if (split > 1) {
+                if (lane == 0)
+                    for (int r = 0; r < split; ++r)
+                        if (r != (int)rank) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, (uint32_t)r));
                 if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane)) break;
             }
 
 #pragma unroll 1
             for (int c = 0; c < BN / kCols; ++c) {
+                if (split > 1 && c % split != (int)rank) continue;
                 uint32_t v[kCols];
                 if (KB > 0) {
                     ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                     if constexpr (OUT == 0)
                         ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                     ptx::tmem_ld_wait();
-                    if (c == BN / kCols - 1) {
+                    if (split == 1 && c == BN / kCols - 1) {
                         // accumulator fully read: hand it back to the MMA warp
                         ptx::tc_fence_before();
                         __syncwarp();
@@ -442,30 +453,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
                 }
-                // split-K: add the other ranks' partials, in rank order
-                for (int r = 1; r < split; ++r) {
+                if (split > 1) {
+                    // add the other ranks' partials to this rank's own, in ascending
+                    // rank order: a fixed order, so the result is deterministic
+                    for (int r = 0; r < split; ++r) {
+                        if (r == (int)rank) continue;
+                        // all of the chunk's remote loads in flight at once, then the adds
+                        uint32_t x[kCols];
 #pragma unroll
-                    for (int j = 0; j < kCols / 4; ++j) {
-                        const int g = c * (kCols / 4) + j;  // 16-byte column group
-                        const uint32_t addr = ptx::mapa(sA + (uint32_t)((g * kBM + row_in_tile) * 16), (uint32_t)r);
-                        uint32_t x0, x1, x2, x3;
-                        ptx::ld_cluster_v4(addr, x0, x1, x2, x3);
-                        fadd_bits(v[4 * j], x0);
-                        fadd_bits(v[4 * j + 1], x1);
-                        fadd_bits(v[4 * j + 2], x2);
-                        fadd_bits(v[4 * j + 3], x3);
+                        for (int j = 0; j < kCols / 4; ++j) {
+                            const int g = c * (kCols / 4) + j;  // 16-byte column group
+                            ptx::ld_cluster_v4(ptx::mapa(sA + (uint32_t)((g * kBM + row_in_tile) * 16), (uint32_t)r),
+                                               x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                     }
                 }
                 store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, row0);
             }
             if (split > 1) {
-                // every other rank's partial has been read
+                // this rank has read every partial it needs; wait until the others
+                // have read this rank's before its shared memory may go away
                 __syncwarp();
                 if (lane == 0)
-                    for (int r = 1; r < split; ++r) ptx::mbar_arrive_cluster(ptx::mapa(red_done_bar, (uint32_t)r));
+                    for (int r = 0; r < split; ++r)
+                        if (r != (int)rank) ptx::mbar_arrive_cluster(ptx::mapa(red_done_bar, (uint32_t)r));
+                warp_wait(red_done_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceDone, lane);
             }
         }
-        if (lane == 0) ptx::bulk_wait_group<0>();
+        // the staging buffers must have been read before shared memory goes
+        // away; the global writes themselves complete with the grid
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
         __syncwarp();
     }
 

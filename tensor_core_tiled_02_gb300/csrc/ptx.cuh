@@ -97,10 +97,25 @@ __device__ __forceinline__ void cluster_sync() {
 
 __device__ __forceinline__ void ld_cluster_v4(uint32_t cluster_addr, uint32_t& a, uint32_t& b, uint32_t& c,
                                               uint32_t& d) {
+    // volatile keeps it after the barrier wait that publishes the data; no
+    // memory clobber, so a run of these loads can be in flight together
     asm volatile("ld.shared::cluster.v4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(a), "=r"(b), "=r"(c), "=r"(d)
-                 : "r"(cluster_addr)
-                 : "memory");
+                 : "r"(cluster_addr));
+}
+
+// ---- programmatic dependent launch ----------------------------------------------
+
+// Block until the grids this one depends on (the previous kernel in the
+// stream, when launched with programmatic serialisation) have completed and
+// their memory is visible.  A no-op without such a dependency.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next grid in the stream start launching (its own prologue may then
+// overlap the rest of this grid; it still waits for this grid's completion
+// before touching memory).
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---- fences -----------------------------------------------------------------

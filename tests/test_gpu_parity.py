@@ -73,10 +73,11 @@ def test_ragged_shapes(M, N, K, out_dtype):
     check_full(a, b, out_dtype, f"ragged {M}x{N}x{K}")
 
 
-# every ring the shared memory holds: 6 buffers at tile_n 128, 4 at 256
+# every ring the shared memory holds: 8 buffers at tile_n 64, 6 at 128, 4 at 256
+MAX_SLOTS = {64: 8, 128: 6, 256: 4}
 VARIANTS = [dict(tile_n=t, stages=s, release=r)
-            for t in (128, 256) for s in (1, 2, 3, 4, 5, 6) for r in (0, 1, 2)
-            if r < s and s + r <= (6 if t == 128 else 4)]
+            for t in (64, 128, 256) for s in range(1, 9) for r in (0, 1, 2)
+            if r < s and s + r <= MAX_SLOTS[t] and (t != 64 or s in (1, 3, 8))]
 
 
 @pytest.mark.parametrize("cfg", VARIANTS, ids=lambda c: f"n{c['tile_n']}s{c['stages']}r{c['release']}")
@@ -88,7 +89,7 @@ def test_pipeline_variants(cfg):
         check_full(a, b, out_dtype, f"variant {cfg} out {out_dtype}")
 
 
-@pytest.mark.parametrize("tile_n", [128, 256])
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
 def test_persistent_many_tiles_per_cta(tile_n):
     """A handful of CTAs each walk many tiles: the ring and both TMEM
     accumulators wrap many times across tile boundaries."""
@@ -97,7 +98,7 @@ def test_persistent_many_tiles_per_cta(tile_n):
     check_full(a, b, 0, f"persistent tile_n={tile_n}")
 
 
-SPLITS = [(2, 128, 0), (2, 256, 1), (3, 128, 0), (4, 128, 1), (8, 128, 0), (5, 256, 0)]
+SPLITS = [(2, 128, 0), (2, 256, 1), (3, 128, 0), (4, 128, 1), (8, 128, 0), (5, 256, 0), (2, 64, 0), (3, 64, 1)]
 
 
 @pytest.mark.parametrize("split,tile_n,out_dtype", SPLITS)
