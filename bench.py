@@ -41,7 +41,8 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (fp16 in, fp32 acc) at 8192³; % of GB300 dense FP16 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["tensor_core_tiled_02_gb300/csrc/gemm_kernel.cuh", "tensor_core_tiled_02_gb300/csrc/ptx.cuh",
+KERNEL_SOURCES = ["tensor_core_tiled_02_gb300/csrc/gemm_common.cuh", "tensor_core_tiled_02_gb300/csrc/gemm_kernel.cuh",
+                  "tensor_core_tiled_02_gb300/csrc/gemm_pair_kernel.cuh", "tensor_core_tiled_02_gb300/csrc/ptx.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_f16.cu"]
 
 
@@ -299,7 +300,7 @@ def workload_config(w, plan) -> dict:
            "inputs": f"A ~ {w.a_dist[0]}({w.a_dist[1]:g}), B ~ {w.b_dist[0]}({w.b_dist[1]:g}), fp16, seeds 0/1",
            "l2": "inputs rotated over 3 copies, each larger than L2 (A+B+C > 126 MB)"}
     if plan is not None:
-        cfg["plan"] = {k: plan[k] for k in ("tile_m", "tile_n", "tile_k", "stages", "release", "slots", "split", "grid",
+        cfg["plan"] = {k: plan[k] for k in ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "release", "slots", "split", "grid",
                                             "raster_group", "num_tiles", "k_steps")}
     return cfg
 

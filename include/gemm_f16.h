@@ -63,6 +63,7 @@ typedef enum {
 
 /* What the planner chose for one problem (gemm_f16_plan). */
 typedef struct {
+    int cta_group;              /* 1: one CTA per tile; 2: a CTA pair (two SMs) per tile */
     int tile_m, tile_n, tile_k; /* output tile and K step (elements) */
     int tiles_m, tiles_n;       /* ceil(M/tile_m), ceil(N/tile_n) */
     int num_tiles;              /* tiles_m * tiles_n: one owner CTA each */
@@ -88,6 +89,8 @@ typedef struct {
     int raster_group;      /* 0 or >= 1 */
     long long wait_limit;  /* 0 = about one second; else clock cycles one device wait may take */
     int split;             /* 0 = planner default; 1 = no split-K; 2..8 = CTAs per tile along K */
+    int cta_group;         /* 0 = planner default; 1 = one CTA per tile; 2 = CTA pairs
+                              (256 x 256 tiles; needs tile_n 0 or 256 and no split) */
     int inject_stall;      /* test hook: 1 makes every CTA's producer issue no loads, so
                               the MMA warp's bounded wait runs out and the kernel reports
                               GEMM_ERR_DEVICE_TIMEOUT instead of finishing.  0 in normal use. */

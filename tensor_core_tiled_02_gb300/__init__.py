@@ -34,7 +34,7 @@ EXPORTED = ["gemm_f16", "gemm_f16_plan", "gemm_f16_set_config", "gemm_f16_get_co
 
 class GemmPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
-        "tile_m", "tile_n", "tile_k", "tiles_m", "tiles_n", "num_tiles", "k_steps", "stages",
+        "cta_group", "tile_m", "tile_n", "tile_k", "tiles_m", "tiles_n", "num_tiles", "k_steps", "stages",
         "release", "slots", "split", "grid", "raster_group", "smem_bytes", "tmem_cols", "threads")]
 
     def as_dict(self) -> dict:
@@ -44,7 +44,8 @@ class GemmPlan(ctypes.Structure):
 class GemmConfig(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("release", ctypes.c_int),
                 ("grid", ctypes.c_int), ("raster_group", ctypes.c_int),
-                ("wait_limit", ctypes.c_longlong), ("split", ctypes.c_int), ("inject_stall", ctypes.c_int)]
+                ("wait_limit", ctypes.c_longlong), ("split", ctypes.c_int), ("cta_group", ctypes.c_int),
+                ("inject_stall", ctypes.c_int)]
 
 
 class GemmError(RuntimeError):

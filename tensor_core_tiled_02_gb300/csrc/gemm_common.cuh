@@ -1,0 +1,181 @@
+// Pieces shared by the fp16 GEMM kernels (one CTA per tile, and the CTA pair
+// of gemm_pair_kernel.cuh): tile constants, launch parameters, descriptors,
+// the grouped raster, bounded mbarrier waits and the epilogue's chunk store.
+#pragma once
+
+#include <cuda.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace tcgemm {
+
+constexpr int kBM = 128;       // tile rows = M of one cta_group::1 MMA = TMEM lanes
+constexpr int kBK = 64;        // K per pipeline step: one 128-byte swizzle row of fp16
+constexpr int kUmmaK = 16;     // K of one tcgen05.mma with 16-bit operands
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kMaxStages = 8;
+constexpr int kMaxSplit = 8;   // portable cluster size
+constexpr int kBoxBytes = kBK * 64 * 2;  // one 64 x 64 fp16 box of B: 8 KiB
+
+// Status word written by a CTA whose bounded wait ran out (first writer wins).
+enum WaitSite : unsigned {
+    kSiteNone = 0,
+    kSiteProducerEmpty = 1,
+    kSiteMmaFull = 2,
+    kSiteMmaTmemEmpty = 3,
+    kSiteEpilogueTmemFull = 4,
+    kSiteDrain = 5,
+    kSiteReduceReady = 6,
+    kSiteReduceDone = 7,
+};
+
+__device__ unsigned int g_status;
+
+struct KernelParams {
+    int M, N, K;
+    int tiles_m, tiles_n, k_blocks;
+    int raster_group;      // m-blocks per raster group
+    int slots;             // ring buffers = stages in flight + release depth, 1 .. kMaxStages
+    int release;           // extra release depth, 0 .. slots-1
+    int split;             // CTAs (one cluster) sharing a tile along K; 1 = no split
+    long long wait_limit;  // clock cycles a single wait may take before giving up
+    int inject;            // test hook: 1 = the producer issues no loads at all
+};
+
+template <int BN, int OUT>
+struct Layout {
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile N");
+    static constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
+    static constexpr int kBBytes = kBK * BN * 2;   // BN/64 boxes of 8 KiB
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kOutCols = OUT == 0 ? 64 : 32;  // columns in one 128-byte output row
+    static constexpr int kStagingBytes = 32 * 128;       // one warp's 32 rows x 128 bytes
+    static constexpr int kTmemCols = 2 * BN;             // two accumulators
+    static constexpr int kPartialBytes = kBM * BN * 4;   // one fp32 partial tile (split-K)
+    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain, red_ready, red_done
+    static constexpr int kNumBars = 2 * kMaxStages + 7;
+    static constexpr int kFixedBytes = 4 * 2 * kStagingBytes + kNumBars * 8 + 16;
+    static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
+};
+
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, A K-major, B
+// MN-major (B is [K,N] with N contiguous), M = 128, N = BN.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n) {
+    return (1u << 4)                            // D format: fp32
+           | (0u << 7) | (0u << 10)             // A, B format: fp16
+           | (0u << 15)                         // A: K-major
+           | (1u << 16)                         // B: MN-major
+           | ((uint32_t)(n >> 3) << 17)         // N / 8
+           | ((uint32_t)(m >> 4) << 24);        // M / 16
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand.
+// lbo/sbo in bytes; version 1 (tcgen05); swizzle mode 2 = 128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Grouped raster: groups of `g` m-blocks; inside a group the m-block varies
+// fastest, so consecutive tile ids share B columns and a few A rows in L2.
+__device__ __forceinline__ void tile_coords(int t, const KernelParams& p, int& mb, int& nb) {
+    const int g = p.raster_group;
+    const int per_group = g * p.tiles_n;
+    const int grp = t / per_group;
+    const int first_m = grp * g;
+    const int gm = min(p.tiles_m - first_m, g);
+    const int r = t - grp * per_group;
+    mb = first_m + r % gm;
+    nb = r / gm;
+}
+
+__device__ __forceinline__ void record_timeout(unsigned site) { atomicCAS(&g_status, 0u, site); }
+
+// Bounded wait on an mbarrier phase.  Gives up (returning false) when the
+// CTA-wide abort flag is raised or, after `limit` cycles, raises it itself.
+// kClusterAcquire: acquire at cluster scope (the data was written by another
+// CTA of the cluster before it arrived).
+template <bool kClusterAcquire = false>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             long long limit, unsigned site) {
+    auto probe = [&]() {
+        return kClusterAcquire ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    };
+    if (probe()) return true;
+    const long long t0 = clock64();
+    while (!probe()) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            *abort_flag = 1;
+            record_timeout(site);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Bounded wait that ignores the abort flag: used after an abort to let the
+// CTA's own asynchronous copies and MMAs land before it exits.
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > limit) {
+            record_timeout(kSiteDrain);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Lane 0 waits, the warp follows its verdict.
+template <bool kClusterAcquire = false>
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, long long limit,
+                                          unsigned site, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = wait_bounded<kClusterAcquire>(bar, parity, abort_flag, limit, site);
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// One 128-byte-wide column chunk of a warp's 32 output rows: convert, write
+// to the warp's staging buffer in the 128-byte swizzle the C tensor map
+// expects (16-byte chunk j of row `lane` at chunk j ^ (lane % 8)), fence for
+// the async proxy and TMA-store it.  Staging is double-buffered per warp.
+template <int OUT>
+__device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 32], const CUtensorMap* tmC,
+                                            uint32_t staging, int& nstore, int lane, int x, int y) {
+    const uint32_t stg = staging + (uint32_t)((nstore & 1) * 4096);
+    // the store issued from this buffer two rounds ago must have read it
+    if (lane == 0) ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+    const uint32_t row_addr = stg + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t w0, w1, w2, w3;
+        if constexpr (OUT == 0) {
+            w0 = ptx::pack_f16x2(v[8 * j + 0], v[8 * j + 1]);
+            w1 = ptx::pack_f16x2(v[8 * j + 2], v[8 * j + 3]);
+            w2 = ptx::pack_f16x2(v[8 * j + 4], v[8 * j + 5]);
+            w3 = ptx::pack_f16x2(v[8 * j + 6], v[8 * j + 7]);
+        } else {
+            w0 = v[4 * j + 0];
+            w1 = v[4 * j + 1];
+            w2 = v[4 * j + 2];
+            w3 = v[4 * j + 3];
+        }
+        ptx::st_shared_v4(row_addr + ((uint32_t)(j ^ (lane & 7)) << 4), w0, w1, w2, w3);
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        ptx::tma_store_2d(tmC, stg, x, y);
+        ptx::bulk_commit_group();
+    }
+    ++nstore;
+}
+
+__device__ __forceinline__ void fadd_bits(uint32_t& acc, uint32_t add) {
+    acc = __float_as_uint(__uint_as_float(acc) + __uint_as_float(add));
+}
+
+}  // namespace tcgemm

@@ -11,6 +11,7 @@
 
 #include "gemm_f16.h"
 #include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 
 namespace {
 
@@ -27,7 +28,7 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int cc = 0;
-    bool attr_set[3][2] = {};  // [tile_n 64 / 128 / 256][out_dtype]
+    bool attr_set[4][2] = {};  // [tile_n 64 / 128 / 256, CTA pair][out_dtype]
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -70,6 +71,8 @@ int check_config(const gemm_config& c) {
     if (c.grid < 0 || c.raster_group < 0 || c.wait_limit < 0) return GEMM_ERR_CONFIG;
     if (c.inject_stall != 0 && c.inject_stall != 1) return GEMM_ERR_CONFIG;
     if (c.split < 0 || c.split > kMaxSplit) return GEMM_ERR_CONFIG;
+    if (c.cta_group < 0 || c.cta_group > 2) return GEMM_ERR_CONFIG;
+    if (c.cta_group == 2 && ((c.tile_n != 0 && c.tile_n != 256) || c.split > 1)) return GEMM_ERR_CONFIG;
     return GEMM_OK;
 }
 
@@ -81,9 +84,29 @@ int smem_for(int tile_n, int out_dtype, int slots) {
     return out_dtype == GEMM_OUT_F16 ? Layout<128, 0>::smem_bytes(slots) : Layout<128, 1>::smem_bytes(slots);
 }
 
+// Shared memory to request so that no SM ever holds more CTAs of this launch
+// than its 512 TMEM columns serve at once: a CTA of a cluster left waiting in
+// tcgen05.alloc for columns held by another cluster's CTA could otherwise
+// wait on a peer that waits in turn.  (228 KiB of shared memory per SM.)
+int smem_request(int smem_bytes, int tmem_cols) {
+    const int max_ctas = 512 / tmem_cols;
+    const int floor_bytes = 233472 / (max_ctas + 1) + 1;
+    return smem_bytes > floor_bytes ? smem_bytes : floor_bytes;
+}
+
+int smem_for_pair(int out_dtype, int slots) {
+    return out_dtype == GEMM_OUT_F16 ? PairLayout<0>::smem_bytes(slots) : PairLayout<1>::smem_bytes(slots);
+}
+
 int max_slots_for(int tile_n, int out_dtype) {
     int s = kMaxStages;
     while (s > 1 && smem_for(tile_n, out_dtype, s) > kSmemLimit) --s;
+    return s;
+}
+
+int max_slots_for_pair(int out_dtype) {
+    int s = kMaxStages;
+    while (s > 1 && smem_for_pair(out_dtype, s) > kSmemLimit) --s;
     return s;
 }
 
@@ -116,6 +139,49 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
     p->tiles_n = ceil_div(N, tn);
     p->num_tiles = p->tiles_m * p->tiles_n;
     p->k_steps = ceil_div(K, kBK);
+
+    // CTA pair (cta_group::2, 256 x 256 tiles on two SMs): when the wide tile
+    // wins and no split is wanted, if its waves cost no more than 1/0.9 of the
+    // single-CTA waves (it moves a third less operand data per SM and step).
+    int cg = cfg.cta_group;
+    if (cg == 0) {
+        cg = 1;
+        if (tn == 256 && cfg.tile_n == 0 && cfg.split <= 1 && p->k_steps > 0 && num_sms >= 2) {
+            const long long pair_tiles = (long long)ceil_div(M, 2 * kBM) * ceil_div(N, 256);
+            const long long w_pair = (pair_tiles + num_sms / 2 - 1) / (num_sms / 2);
+            const long long w_one = ((long long)p->num_tiles + num_sms - 1) / num_sms;
+            const long long tiles128 = (long long)tiles_m * ceil_div(N, 128);
+            if (w_pair * 9 <= w_one * 10 && 2 * tiles128 > num_sms) cg = 2;
+        }
+    }
+    if (cg == 2) {
+        if (p->k_steps == 0 || num_sms < 2) return GEMM_ERR_CONFIG;
+        p->cta_group = 2;
+        p->tile_m = 2 * kBM;
+        p->tile_n = 256;
+        p->tiles_m = ceil_div(M, 2 * kBM);
+        p->tiles_n = ceil_div(N, 256);
+        p->num_tiles = p->tiles_m * p->tiles_n;
+        p->split = 1;
+        int pairs = p->num_tiles < num_sms / 2 ? p->num_tiles : num_sms / 2;
+        if (cfg.grid > 0 && cfg.grid / 2 < pairs) pairs = cfg.grid / 2 > 0 ? cfg.grid / 2 : 1;
+        p->grid = 2 * pairs;
+        const int d = cfg.release;
+        const int max_slots = max_slots_for_pair(out_dtype);
+        int s = cfg.stages > 0 ? cfg.stages : max_slots - d;
+        if (s <= d || s + d > max_slots) return GEMM_ERR_CONFIG;
+        const long long steps_per_cta = (long long)p->k_steps * ceil_div(p->num_tiles, pairs);
+        if (steps_per_cta < s) s = (int)(steps_per_cta > d ? steps_per_cta : d + 1);
+        p->stages = s;
+        p->release = d;
+        p->slots = s + d;
+        p->raster_group = cfg.raster_group > 0 ? cfg.raster_group : 8;
+        p->tmem_cols = 512;
+        p->smem_bytes = smem_request(smem_for_pair(out_dtype, p->slots), p->tmem_cols);
+        p->threads = kThreads;
+        return GEMM_OK;
+    }
+    p->cta_group = 1;
 
     int split = cfg.split;
     if (split == 0) {
@@ -156,8 +222,8 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
     p->release = d;
     p->slots = s + d;
     p->raster_group = cfg.raster_group > 0 ? cfg.raster_group : 16;
-    p->smem_bytes = smem_for(tn, out_dtype, p->slots);
     p->tmem_cols = 2 * tn;
+    p->smem_bytes = smem_request(smem_for(tn, out_dtype, p->slots), p->tmem_cols);
     p->threads = kThreads;
     return GEMM_OK;
 }
@@ -205,6 +271,40 @@ int device_info(DeviceInfo** out) {
         d.ready = true;
     }
     *out = &d;
+    return GEMM_OK;
+}
+
+template <int OUT>
+int launch_pair(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
+    auto kern = gemm_f16_pair_kernel<OUT>;
+    bool& attr_done = dev.attr_set[3][OUT];
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        attr_done = true;
+    }
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(plan.grid, 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = plan.smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&lc, kern, ta, tb, tc, kp);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
     return GEMM_OK;
 }
 
@@ -304,6 +404,9 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
     kp.inject = cfg.inject_stall;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan.cta_group == 2)
+        return out_dtype == GEMM_OUT_F16 ? launch_pair<0>(plan, ta, tb, tc, kp, s, *dev)
+                                         : launch_pair<1>(plan, ta, tb, tc, kp, s, *dev);
     if (plan.tile_n == 256)
         return out_dtype == GEMM_OUT_F16 ? launch<256, 0>(plan, ta, tb, tc, kp, s, *dev)
                                          : launch<256, 1>(plan, ta, tb, tc, kp, s, *dev);
@@ -358,7 +461,7 @@ const char* gemm_f16_strerror(int code) {
         case GEMM_ERR_DTYPE: return "out_dtype must be GEMM_OUT_F16 (0) or GEMM_OUT_F32 (1)";
         case GEMM_ERR_ALIGN: return "pointers must be 16-byte aligned and N, K multiples of 8";
         case GEMM_ERR_ALIAS: return "C overlaps A or B";
-        case GEMM_ERR_CONFIG: return "invalid tuning config (stages must exceed release; tile_n 128 or 256; ring must fit shared memory)";
+        case GEMM_ERR_CONFIG: return "invalid tuning config for this problem (stages must exceed release; tile_n 64, 128 or 256; ring must fit shared memory; split and CTA pairs need K steps)";
         case GEMM_ERR_TMAP: return "the driver refused a TMA tensor-map encoding";
         case GEMM_ERR_LAUNCH: return "kernel launch failed";
         case GEMM_ERR_CUDA: return "no usable CUDA device or driver";

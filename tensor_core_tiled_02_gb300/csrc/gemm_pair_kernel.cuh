@@ -1,0 +1,251 @@
+// The fp16 GEMM on a CTA pair (cta_group::2): a cluster of two CTAs on two
+// SMs owns each 256 x 256 output tile.
+//
+// Same method as gemm_kernel.cuh (parallel grid of tiles, K pipeline through
+// an mbarrier-guarded shared-memory ring, fp32 accumulator in TMEM, drain
+// through shared memory and TMA; "Quickstart: GPU", section "Pipelining: a
+// matmul kernel"), with the tile split over two SMs:
+//   - CTA r (r = rank in the cluster) loads A rows [256 mb + 128 r, +128) and
+//     B columns [256 nb + 128 r, +128) of each K step: 32 KiB per step each,
+//     where a 128 x 256 tile on one SM needs 48 KiB;
+//   - one thread of the even CTA issues tcgen05.mma.cta_group::2 with M = 256,
+//     N = 256: each SM's tensor core takes its 128 rows of A from its own
+//     shared memory and the two halves of B from both, and writes its 128
+//     rows of D into its own TMEM;
+//   - both CTAs' loads count on the even CTA's `full` barrier (the leader arms
+//     it for both); the MMA commits release the slot in both CTAs and signal
+//     both epilogues (multicast); both CTAs' epilogue warps hand the
+//     accumulator back on the even CTA's `tmem_empty` barrier;
+//   - each CTA's epilogue drains its own 128 x 256 block exactly as the
+//     single-CTA kernel does.
+// Persistent: cluster c walks pair tiles c, c + clusters, ... in the grouped
+// raster.  Programmatic dependent launch as in the single-CTA kernel.
+#pragma once
+
+#include "gemm_common.cuh"
+
+namespace tcgemm {
+
+constexpr int kPairBM = 256;  // tile rows per pair (MMA M)
+constexpr int kPairBN = 256;  // tile columns per pair (MMA N)
+
+template <int OUT>
+struct PairLayout {
+    static constexpr int kABytes = kBM * kBK * 2;          // this CTA's 128 rows: 16 KiB
+    static constexpr int kBBytes = kBK * (kPairBN / 2) * 2;  // this CTA's 128 columns: 16 KiB
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kOutCols = OUT == 0 ? 64 : 32;
+    static constexpr int kStagingBytes = 32 * 128;
+    static constexpr int kTmemCols = 2 * kPairBN;  // two 256-column accumulators: all 512
+    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain
+    static constexpr int kNumBars = 2 * kMaxStages + 5;
+    static constexpr int kFixedBytes = 4 * 2 * kStagingBytes + kNumBars * 8 + 16;
+    static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
+};
+
+template <int OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
+    using L = PairLayout<OUT>;
+    constexpr int kCols = L::kOutCols;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw);
+    const int S = p.slots;
+    const uint32_t sA = base;
+    const uint32_t sB = sA + S * L::kABytes;
+    const uint32_t sC = sB + S * L::kBBytes;
+    const uint32_t bar0 = sC + 4 * 2 * L::kStagingBytes;
+    const uint32_t misc_off = (bar0 - base) + L::kNumBars * 8;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + misc_off);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + misc_off + 4);
+
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kMaxStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kMaxStages + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = ptx::cluster_ctarank();  // 0: leader (issues the MMAs), 1: peer
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(full_bar(s), 1);   // the leader's arrive; both CTAs' bytes
+            ptx::mbar_init(empty_bar(s), 1);  // the leader's multicast commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(tfull_bar(a), 1);   // the leader's multicast commit
+            ptx::mbar_init(tempty_bar(a), 8);  // 4 epilogue warps in each CTA
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tmap(&tmA);
+        ptx::prefetch_tmap(&tmB);
+        ptx::prefetch_tmap(&tmC);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc_pair(ptx::smem_addr((const void*)tmem_slot), L::kTmemCols);
+        ptx::tmem_relinquish_pair();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    // both CTAs' barriers are initialised before either signals the other
+    ptx::cluster_sync();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    ptx::grid_dependency_wait();
+    ptx::grid_launch_dependents();
+
+    const int num_tiles = p.tiles_m * p.tiles_n;  // in 256 x 256 pair tiles
+    const int first_tile = blockIdx.x >> 1;
+    const int tile_stride = gridDim.x >> 1;
+    const int KB = p.k_blocks;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (both CTAs) ----------------
+        if (lane == 0 && KB > 0 && p.inject == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int t = first_tile; ok && t < num_tiles; t += tile_stride) {
+                int mb, nb;
+                tile_coords(t, p, mb, nb);
+                const int m0 = mb * kPairBM + (int)rank * kBM;
+                const int n0 = nb * kPairBN + (int)rank * (kPairBN / 2);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb_local = full_bar(stage);
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * L::kStageBytes);
+                    const uint32_t fb = ptx::mapa(fb_local, 0);
+                    ptx::tma_load_2d_pair(sA + stage * L::kABytes, &tmA, fb, kb * kBK, m0);
+                    ptx::tma_load_2d_pair(sB + stage * L::kBBytes, &tmB, fb, n0, kb * kBK);
+                    ptx::tma_load_2d_pair(sB + stage * L::kBBytes + kBoxBytes, &tmB, fb, n0 + 64, kb * kBK);
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // the leader's full barriers count both CTAs' bytes: let every armed
+            // phase land before shared memory goes away
+            if (rank == 0)
+                for (int s = 0; s < S; ++s)
+                    if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_phase >> s) & 1u, p.wait_limit);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (leader only) ----------------
+        if (lane == 0 && rank == 0 && KB > 0) {
+            constexpr uint32_t idesc = make_idesc(kPairBM, kPairBN);
+            int stage = 0;
+            uint32_t phase = 0;
+            long long it = 0;
+            int tl = 0;
+            bool ok = true;
+            for (int t = first_tile; ok && t < num_tiles; t += tile_stride, ++tl) {
+                const int acc = tl & 1;
+                const uint32_t aph = (tl >> 1) & 1;
+                if (!wait_bounded<true>(tempty_bar(acc), aph ^ 1u, abort_flag, p.wait_limit, kSiteMmaTmemEmpty)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kPairBN);
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit, kSiteMmaFull)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a0 = sA + stage * L::kABytes;
+                    const uint32_t b0 = sB + stage * L::kBBytes;
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        const uint64_t ad = sw128_desc(a0 + k * (kUmmaK * 2), 16, 1024);
+                        const uint64_t bd = sw128_desc(b0 + k * (kUmmaK * 128), kBoxBytes, 1024);
+                        ptx::mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                    }
+                    if (it >= p.release) {
+                        int rs = stage - p.release;
+                        if (rs < 0) rs += S;
+                        ptx::mma_commit_pair_multicast(empty_bar(rs), 0x3);
+                    }
+                    ++it;
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit_pair_multicast(tfull_bar(acc), 0x3);
+            }
+            ptx::mma_commit_pair(drain_bar);
+            wait_drain(drain_bar, 0, p.wait_limit);
+        }
+    } else {
+        // ---------------- epilogue (both CTAs): own 128 rows x 256 columns ----------------
+        const int q = warp & 3;
+        const uint32_t staging = sC + (uint32_t)(q * 2 * L::kStagingBytes);
+        int tl = 0;
+        int nstore = 0;
+        for (int t = first_tile; t < num_tiles; t += tile_stride, ++tl) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            const int acc = tl & 1;
+            const uint32_t aph = (tl >> 1) & 1;
+            if (KB > 0) {
+                if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane))
+                    break;
+                ptx::tc_fence_after();
+            }
+            const int row0 = mb * kPairBM + (int)rank * kBM + q * 32;
+            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPairBN);
+#pragma unroll 1
+            for (int c = 0; c < kPairBN / kCols; ++c) {
+                uint32_t v[kCols];
+                if (KB > 0) {
+                    ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                    if constexpr (OUT == 0)
+                        ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                    ptx::tmem_ld_wait();
+                    if (c == kPairBN / kCols - 1) {
+                        // this CTA's half of the accumulator is read: tell the leader
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
+                }
+                store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * kPairBN + c * kCols, row0);
+            }
+        }
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    // neither CTA leaves while the other may still signal into it
+    ptx::cluster_sync();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc_pair(tmem_base, L::kTmemCols);
+    }
+}
+
+}  // namespace tcgemm

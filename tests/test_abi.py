@@ -84,10 +84,12 @@ def test_plan_matches_the_tiling_arithmetic(lib):
     for name, w in WORKLOADS.items():
         p = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, num_sms=152)
         assert p["k_steps"] == want_k_steps[name] == w.K // 64
-        assert p["tile_m"] == 128 and p["tile_k"] == 64
-        assert p["tiles_m"] == -(-w.M // 128) and p["tiles_n"] == -(-w.N // p["tile_n"])
+        assert p["tile_m"] == 128 * p["cta_group"] and p["tile_k"] == 64
+        assert p["tiles_m"] == -(-w.M // p["tile_m"]) and p["tiles_n"] == -(-w.N // p["tile_n"])
         assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
-        if p["split"] == 1:
+        if p["cta_group"] == 2:  # one cluster of two CTAs per pair tile, persistent
+            assert p["grid"] == 2 * min(p["num_tiles"], 76) and p["split"] == 1
+        elif p["split"] == 1:
             assert p["grid"] == min(p["num_tiles"], 152)
         else:  # one tile per cluster of `split` CTAs
             assert p["grid"] == p["num_tiles"] * p["split"] <= 152
@@ -96,15 +98,59 @@ def test_plan_matches_the_tiling_arithmetic(lib):
         assert p["smem_bytes"] <= 232448
     # the 256^3 case is 2 x 2 tiles of 128 x 128 with 4 K steps
     p = tc.gemm_f16_plan(256, 256, 256, 0, num_sms=152)
-    assert (p["tiles_m"], p["tiles_n"], p["tile_n"], p["k_steps"]) == (2, 2, 128, 4)
-    # the big square problem takes the wide tile
-    assert tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152)["tile_n"] == 256
-    # long K: 128 wide tiles in one wave beat 256 narrow ones in two
+    assert (p["tiles_m"], p["tiles_n"], p["tile_n"], p["k_steps"], p["cta_group"]) == (2, 2, 128, 4, 1)
+    # the big square problem takes 256 x 256 tiles on CTA pairs
+    p = tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152)
+    assert (p["cta_group"], p["tile_m"], p["tile_n"], p["num_tiles"], p["grid"]) == (2, 256, 256, 1024, 152)
+    # long K: 64 pair tiles in one wave
     p = tc.gemm_f16_plan(2048, 2048, 32768, 1, num_sms=152)
-    assert (p["tile_n"], p["num_tiles"], p["split"], p["grid"]) == (256, 128, 1, 128)
+    assert (p["cta_group"], p["num_tiles"], p["split"], p["grid"]) == (2, 64, 1, 128)
+    # without pairs: 128 wide tiles in one wave beat 256 narrow ones in two
+    try:
+        tc.gemm_f16_set_config(cta_group=1)
+        p = tc.gemm_f16_plan(2048, 2048, 32768, 1, num_sms=152)
+        assert (p["tile_n"], p["num_tiles"], p["split"], p["grid"]) == (256, 128, 1, 128)
+    finally:
+        tc.gemm_f16_set_config()
     # skinny: 64 narrow tiles would fill under half the SMs, so two CTAs share each along K
     p = tc.gemm_f16_plan(128, 8192, 8192, 0, num_sms=152)
     assert (p["tile_n"], p["num_tiles"], p["split"], p["grid"]) == (128, 64, 2, 128)
+
+
+def test_cta_pair_planning(lib):
+    try:
+        tc.gemm_f16_set_config(cta_group=2)
+        p = tc.gemm_f16_plan(600, 520, 776, 0, num_sms=152)
+        assert (p["tile_m"], p["tiles_m"], p["tiles_n"], p["grid"], p["slots"]) == (256, 3, 3, 18, 6)
+        with pytest.raises(tc.GemmError):                       # no K steps to pair on
+            tc.gemm_f16_plan(256, 256, 0, 0, num_sms=152)
+        with pytest.raises(tc.GemmError):
+            tc.gemm_f16_set_config(cta_group=2, split=2)
+        with pytest.raises(tc.GemmError):
+            tc.gemm_f16_set_config(cta_group=2, tile_n=128)
+        with pytest.raises(tc.GemmError):
+            tc.gemm_f16_set_config(cta_group=3)
+        tc.gemm_f16_set_config(cta_group=2, grid=4)
+        assert tc.gemm_f16_plan(1100, 1280, 264, 0, num_sms=152)["grid"] == 4
+    finally:
+        tc.gemm_f16_set_config()
+
+
+def test_tmem_never_oversubscribed(lib):
+    """No SM may hold more CTAs of one launch than 512 TMEM columns serve."""
+    for cfg in ({}, dict(tile_n=64), dict(tile_n=128), dict(split=2), dict(tile_n=64, split=2), dict(cta_group=2)):
+        tc.gemm_f16_set_config(**cfg)
+        try:
+            for M, N, K in [(128, 128, 64), (256, 1024, 2048), (8192, 8192, 8192), (128, 8192, 8192)]:
+                try:
+                    p = tc.gemm_f16_plan(M, N, K, 0, num_sms=152)
+                except tc.GemmError as e:  # e.g. a forced split longer than K
+                    assert e.code == CONFIG
+                    continue
+                ctas_per_sm = 233472 // (p["smem_bytes"] + 1024)
+                assert ctas_per_sm * p["tmem_cols"] <= 512, (cfg, M, N, K, p)
+        finally:
+            tc.gemm_f16_set_config()
 
 
 def test_split_k_planning(lib):
@@ -154,15 +200,18 @@ def test_stages_clamp_and_release_rule(lib):
         assert (p["stages"], p["slots"]) == (2, 2)
         p = tc.gemm_f16_plan(128, 128, 64, 0, num_sms=152)   # 1 step
         assert (p["stages"], p["slots"]) == (1, 1)
-        p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)
+        p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)   # CTA pairs: 32 KiB steps
+        assert (p["cta_group"], p["stages"], p["release"], p["slots"]) == (2, 6, 0, 6)
+        tc.gemm_f16_set_config(cta_group=1)
+        p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)   # one CTA: 48 KiB steps
         assert (p["tile_n"], p["stages"], p["release"], p["slots"]) == (256, 4, 0, 4)
         # the pages' example: max_concurrent_steps=2, delay_release=1 -> 3 buffers
-        tc.gemm_f16_set_config(stages=2, release=1)
+        tc.gemm_f16_set_config(cta_group=1, stages=2, release=1)
         p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)
         assert (p["stages"], p["release"], p["slots"]) == (2, 1, 3)
         p = tc.gemm_f16_plan(128, 128, 64, 0, num_sms=152)   # clamp stops above release
         assert (p["stages"], p["slots"]) == (2, 3)
-        tc.gemm_f16_set_config(release=1)                      # default stages: fill the ring
+        tc.gemm_f16_set_config(cta_group=1, release=1)         # default stages: fill the ring
         p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)
         assert (p["stages"], p["release"], p["slots"]) == (3, 1, 4)
         with pytest.raises(tc.GemmError) as e:
@@ -186,7 +235,7 @@ def test_stages_clamp_and_release_rule(lib):
 
 def test_config_roundtrip(lib):
     try:
-        tc.gemm_f16_set_config(tile_n=128, stages=3, release=1, grid=7, raster_group=4)
+        tc.gemm_f16_set_config(tile_n=128, stages=3, release=1, grid=7, raster_group=4, cta_group=1)
         c = tc.gemm_f16_get_config()
         assert (c["tile_n"], c["stages"], c["release"], c["grid"], c["raster_group"]) == (128, 3, 1, 7, 4)
         p = tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152)

@@ -110,6 +110,30 @@ def test_split_k(split, tile_n, out_dtype):
     check_full(a, b, out_dtype, f"split {split} tile_n {tile_n}")
 
 
+PAIR_VARIANTS = [dict(cta_group=2, stages=s, release=r) for s, r in [(1, 0), (2, 1), (3, 0), (4, 2), (6, 0)]]
+
+
+@pytest.mark.parametrize("cfg", PAIR_VARIANTS, ids=lambda c: f"pair_s{c['stages']}r{c['release']}")
+def test_cta_pair_variants(cfg):
+    """256 x 256 tiles on a CTA pair (cta_group::2): ragged M (half a pair
+    tile past the edge), N and K, every ring depth and release depth."""
+    tc.gemm_f16_set_config(**cfg)
+    a, b = make_inputs(600, 520, 776, ("uniform", 1.0), ("uniform", 1.0), seed_a=7, seed_b=8)
+    for out_dtype in (0, 1):
+        check_full(a, b, out_dtype, f"pair {cfg} out {out_dtype}")
+
+
+def test_cta_pair_persistent_and_tiny():
+    """Two pairs walk 20 pair tiles (both TMEM accumulators wrap); then a
+    problem smaller than one pair tile."""
+    tc.gemm_f16_set_config(cta_group=2, grid=4, raster_group=2)
+    a, b = make_inputs(1100, 1280, 264, ("normal", 1.0), ("normal", 1.0), seed_a=3, seed_b=4)
+    check_full(a, b, 0, "pair persistent")
+    tc.gemm_f16_set_config(cta_group=2)
+    a, b = make_inputs(64, 72, 40, ("normal", 1.0), ("normal", 1.0), seed_a=5, seed_b=6)
+    check_full(a, b, 1, "pair tiny")
+
+
 def test_split_k_is_deterministic():
     tc.gemm_f16_set_config(split=4)
     a, b = make_inputs(128, 1024, 4096, ("uniform", 1.0), ("uniform", 1.0), seed_a=1, seed_b=2)
