@@ -381,7 +381,8 @@ def run_ours(args, w, dist: Dist):
             "traffic": recorded_traffic(w.name, plan),
             "peak_source": f"bf16_tflops (burst) of {peak_src}; fp16 dense rate equals bf16 on this part",
             "frac_of_sustained": achieved / peak_sus,
-            "kernel": f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>",
+            "kernel": (f"gemm_f16_pair_kernel<{w.out_dtype},{plan['tile_k']}>" if plan["cta_group"] == 2
+                       else f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>"),
             "avg_launch_ms": avg_launch_s * 1e3,
         }
         cpu = None

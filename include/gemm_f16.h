@@ -91,6 +91,8 @@ typedef struct {
     int split;             /* 0 = planner default; 1 = no split-K; 2..8 = CTAs per tile along K */
     int cta_group;         /* 0 = planner default; 1 = one CTA per tile; 2 = CTA pairs
                               (256 x 256 tiles; needs tile_n 0 or 256 and no split) */
+    int tile_k;            /* 0 = planner default; K depth of one pipeline step: 64, or 128
+                              (CTA pairs only) */
     int inject_stall;      /* test hook: 1 makes every CTA's producer issue no loads, so
                               the MMA warp's bounded wait runs out and the kernel reports
                               GEMM_ERR_DEVICE_TIMEOUT instead of finishing.  0 in normal use. */

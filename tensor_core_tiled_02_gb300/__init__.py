@@ -44,7 +44,7 @@ class GemmPlan(ctypes.Structure):
 class GemmConfig(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("release", ctypes.c_int),
                 ("grid", ctypes.c_int), ("raster_group", ctypes.c_int),
-                ("wait_limit", ctypes.c_longlong), ("split", ctypes.c_int), ("cta_group", ctypes.c_int),
+                ("wait_limit", ctypes.c_longlong), ("split", ctypes.c_int), ("cta_group", ctypes.c_int), ("tile_k", ctypes.c_int),
                 ("inject_stall", ctypes.c_int)]
 
 

@@ -28,7 +28,7 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int cc = 0;
-    bool attr_set[4][2] = {};  // [tile_n 64 / 128 / 256, CTA pair][out_dtype]
+    bool attr_set[5][2] = {};  // [tile_n 64 / 128 / 256, CTA pair step K 64 / 128][out_dtype]
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -73,6 +73,7 @@ int check_config(const gemm_config& c) {
     if (c.split < 0 || c.split > kMaxSplit) return GEMM_ERR_CONFIG;
     if (c.cta_group < 0 || c.cta_group > 2) return GEMM_ERR_CONFIG;
     if (c.cta_group == 2 && ((c.tile_n != 0 && c.tile_n != 256) || c.split > 1)) return GEMM_ERR_CONFIG;
+    if (c.tile_k != 0 && c.tile_k != 64 && c.tile_k != 128) return GEMM_ERR_CONFIG;
     return GEMM_OK;
 }
 
@@ -94,8 +95,11 @@ int smem_request(int smem_bytes, int tmem_cols) {
     return smem_bytes > floor_bytes ? smem_bytes : floor_bytes;
 }
 
-int smem_for_pair(int out_dtype, int slots) {
-    return out_dtype == GEMM_OUT_F16 ? PairLayout<0>::smem_bytes(slots) : PairLayout<1>::smem_bytes(slots);
+int smem_for_pair(int out_dtype, int step_k, int slots) {
+    if (step_k == 128)
+        return out_dtype == GEMM_OUT_F16 ? PairLayout<0, 128>::smem_bytes(slots)
+                                         : PairLayout<1, 128>::smem_bytes(slots);
+    return out_dtype == GEMM_OUT_F16 ? PairLayout<0, 64>::smem_bytes(slots) : PairLayout<1, 64>::smem_bytes(slots);
 }
 
 int max_slots_for(int tile_n, int out_dtype) {
@@ -104,9 +108,9 @@ int max_slots_for(int tile_n, int out_dtype) {
     return s;
 }
 
-int max_slots_for_pair(int out_dtype) {
+int max_slots_for_pair(int out_dtype, int step_k) {
     int s = kMaxStages;
-    while (s > 1 && smem_for_pair(out_dtype, s) > kSmemLimit) --s;
+    while (s > 1 && smem_for_pair(out_dtype, step_k, s) > kSmemLimit) --s;
     return s;
 }
 
@@ -156,7 +160,11 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
     }
     if (cg == 2) {
         if (p->k_steps == 0 || num_sms < 2) return GEMM_ERR_CONFIG;
+        // 128-deep steps (eight MMAs per barrier wait and commit) unless K is short
+        const int sk = cfg.tile_k > 0 ? cfg.tile_k : (K >= 256 ? 128 : kBK);
         p->cta_group = 2;
+        p->tile_k = sk;
+        p->k_steps = ceil_div(K, sk);
         p->tile_m = 2 * kBM;
         p->tile_n = 256;
         p->tiles_m = ceil_div(M, 2 * kBM);
@@ -167,7 +175,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
         if (cfg.grid > 0 && cfg.grid / 2 < pairs) pairs = cfg.grid / 2 > 0 ? cfg.grid / 2 : 1;
         p->grid = 2 * pairs;
         const int d = cfg.release;
-        const int max_slots = max_slots_for_pair(out_dtype);
+        const int max_slots = max_slots_for_pair(out_dtype, sk);
         int s = cfg.stages > 0 ? cfg.stages : max_slots - d;
         if (s <= d || s + d > max_slots) return GEMM_ERR_CONFIG;
         const long long steps_per_cta = (long long)p->k_steps * ceil_div(p->num_tiles, pairs);
@@ -177,11 +185,12 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
         p->slots = s + d;
         p->raster_group = cfg.raster_group > 0 ? cfg.raster_group : 8;
         p->tmem_cols = 512;
-        p->smem_bytes = smem_request(smem_for_pair(out_dtype, p->slots), p->tmem_cols);
+        p->smem_bytes = smem_request(smem_for_pair(out_dtype, sk, p->slots), p->tmem_cols);
         p->threads = kThreads;
         return GEMM_OK;
     }
     p->cta_group = 1;
+    if (cfg.tile_k != 0 && cfg.tile_k != kBK) return GEMM_ERR_CONFIG;  // deep steps: pairs only
 
     int split = cfg.split;
     if (split == 0) {
@@ -274,11 +283,11 @@ int device_info(DeviceInfo** out) {
     return GEMM_OK;
 }
 
-template <int OUT>
+template <int OUT, int SK>
 int launch_pair(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
-    auto kern = gemm_f16_pair_kernel<OUT>;
-    bool& attr_done = dev.attr_set[3][OUT];
+    auto kern = gemm_f16_pair_kernel<OUT, SK>;
+    bool& attr_done = dev.attr_set[SK == 128 ? 4 : 3][OUT];
     if (!attr_done) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess) {
             cudaGetLastError();
@@ -380,7 +389,7 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
     if (K > 0) {
         rc = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, kBK, kBM);
         if (rc != GEMM_OK) return rc;
-        rc = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, (uint64_t)N, (uint64_t)K, 64, kBK);
+        rc = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, (uint64_t)N, (uint64_t)K, 64, plan.tile_k);
         if (rc != GEMM_OK) return rc;
     }
     if (out_dtype == GEMM_OUT_F16)
@@ -404,9 +413,12 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
     kp.inject = cfg.inject_stall;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan.cta_group == 2 && plan.tile_k == 128)
+        return out_dtype == GEMM_OUT_F16 ? launch_pair<0, 128>(plan, ta, tb, tc, kp, s, *dev)
+                                         : launch_pair<1, 128>(plan, ta, tb, tc, kp, s, *dev);
     if (plan.cta_group == 2)
-        return out_dtype == GEMM_OUT_F16 ? launch_pair<0>(plan, ta, tb, tc, kp, s, *dev)
-                                         : launch_pair<1>(plan, ta, tb, tc, kp, s, *dev);
+        return out_dtype == GEMM_OUT_F16 ? launch_pair<0, 64>(plan, ta, tb, tc, kp, s, *dev)
+                                         : launch_pair<1, 64>(plan, ta, tb, tc, kp, s, *dev);
     if (plan.tile_n == 256)
         return out_dtype == GEMM_OUT_F16 ? launch<256, 0>(plan, ta, tb, tc, kp, s, *dev)
                                          : launch<256, 1>(plan, ta, tb, tc, kp, s, *dev);

@@ -29,10 +29,15 @@ namespace tcgemm {
 constexpr int kPairBM = 256;  // tile rows per pair (MMA M)
 constexpr int kPairBN = 256;  // tile columns per pair (MMA N)
 
-template <int OUT>
+// SK: K depth of one pipeline step, 64 or 128.  A deeper step issues twice
+// the MMAs per barrier wait and per commit, with the same bytes in flight.
+template <int OUT, int SK = kBK>
 struct PairLayout {
-    static constexpr int kABytes = kBM * kBK * 2;          // this CTA's 128 rows: 16 KiB
-    static constexpr int kBBytes = kBK * (kPairBN / 2) * 2;  // this CTA's 128 columns: 16 KiB
+    static_assert(SK == 64 || SK == 128, "step K");
+    static constexpr int kAtomBytes = kBM * 64 * 2;          // 128 rows x one 128-byte swizzle row
+    static constexpr int kABytes = kBM * SK * 2;             // this CTA's 128 rows: SK/64 atoms
+    static constexpr int kBBoxBytes = SK * 64 * 2;           // 64 columns x SK rows of B
+    static constexpr int kBBytes = 2 * kBBoxBytes;           // this CTA's 128 columns of B
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kOutCols = OUT == 0 ? 64 : 32;
     static constexpr int kStagingBytes = 32 * 128;
@@ -43,11 +48,11 @@ struct PairLayout {
     static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
 };
 
-template <int OUT>
+template <int OUT, int SK>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
-    using L = PairLayout<OUT>;
+    using L = PairLayout<OUT, SK>;
     constexpr int kCols = L::kOutCols;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -128,9 +133,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb_local = full_bar(stage);
                     if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * L::kStageBytes);
                     const uint32_t fb = ptx::mapa(fb_local, 0);
-                    ptx::tma_load_2d_pair(sA + stage * L::kABytes, &tmA, fb, kb * kBK, m0);
-                    ptx::tma_load_2d_pair(sB + stage * L::kBBytes, &tmB, fb, n0, kb * kBK);
-                    ptx::tma_load_2d_pair(sB + stage * L::kBBytes + kBoxBytes, &tmB, fb, n0 + 64, kb * kBK);
+#pragma unroll
+                    for (int h = 0; h < SK / 64; ++h)
+                        ptx::tma_load_2d_pair(sA + stage * L::kABytes + h * L::kAtomBytes, &tmA, fb, kb * SK + h * 64,
+                                              m0);
+                    ptx::tma_load_2d_pair(sB + stage * L::kBBytes, &tmB, fb, n0, kb * SK);
+                    ptx::tma_load_2d_pair(sB + stage * L::kBBytes + L::kBBoxBytes, &tmB, fb, n0 + 64, kb * SK);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -171,10 +179,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after();
                     const uint32_t a0 = sA + stage * L::kABytes;
                     const uint32_t b0 = sB + stage * L::kBBytes;
+                    // descriptors of the step's first K slice; later slices add to
+                    // the start-address field (16-byte units, no carry out of it)
+                    const uint64_t ad0 = sw128_desc(a0, 16, 1024);
+                    const uint64_t bd0 = sw128_desc(b0, L::kBBoxBytes, 1024);
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        const uint64_t ad = sw128_desc(a0 + k * (kUmmaK * 2), 16, 1024);
-                        const uint64_t bd = sw128_desc(b0 + k * (kUmmaK * 128), kBoxBytes, 1024);
+                    for (int k = 0; k < SK / kUmmaK; ++k) {
+                        // A K-major: slice k is 32 bytes along the swizzled row of atom k/4.
+                        // B MN-major: slice k is two 8-row groups (2 KiB) further down;
+                        // the two 64-wide column blocks are one box apart.
+                        const uint64_t ad = ad0 + (uint64_t)(((k / 4) * L::kAtomBytes + (k % 4) * (kUmmaK * 2)) >> 4);
+                        const uint64_t bd = bd0 + (uint64_t)((k * (kUmmaK * 128)) >> 4);
                         ptx::mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
                     }
                     if (it >= p.release) {

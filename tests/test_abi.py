@@ -80,11 +80,12 @@ def test_empty_problems_are_noops(lib):
 def test_plan_matches_the_tiling_arithmetic(lib):
     """Sequential steps = K / tile_k for each workload; one CTA per output tile;
     tiles = ceil(M/128) * ceil(N/tile_n)."""
-    want_k_steps = {"gemm_256": 4, "gemm_4096": 64, "gemm_8192": 128, "skinny": 128, "long_k": 512}
+    # sequential steps of 64 (one CTA per tile) or 128 (CTA pairs) along K
+    want_k_steps = {"gemm_256": 4, "gemm_4096": 32, "gemm_8192": 64, "skinny": 128, "long_k": 256}
     for name, w in WORKLOADS.items():
         p = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, num_sms=152)
-        assert p["k_steps"] == want_k_steps[name] == w.K // 64
-        assert p["tile_m"] == 128 * p["cta_group"] and p["tile_k"] == 64
+        assert p["k_steps"] == want_k_steps[name] == w.K // p["tile_k"]
+        assert p["tile_m"] == 128 * p["cta_group"] and p["tile_k"] == 64 * p["cta_group"]
         assert p["tiles_m"] == -(-w.M // p["tile_m"]) and p["tiles_n"] == -(-w.N // p["tile_n"])
         assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
         if p["cta_group"] == 2:  # one cluster of two CTAs per pair tile, persistent
@@ -102,6 +103,7 @@ def test_plan_matches_the_tiling_arithmetic(lib):
     # the big square problem takes 256 x 256 tiles on CTA pairs
     p = tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152)
     assert (p["cta_group"], p["tile_m"], p["tile_n"], p["num_tiles"], p["grid"]) == (2, 256, 256, 1024, 152)
+    assert (p["tile_k"], p["k_steps"], p["slots"]) == (128, 64, 3)
     # long K: 64 pair tiles in one wave
     p = tc.gemm_f16_plan(2048, 2048, 32768, 1, num_sms=152)
     assert (p["cta_group"], p["num_tiles"], p["split"], p["grid"]) == (2, 64, 1, 128)
@@ -121,7 +123,9 @@ def test_cta_pair_planning(lib):
     try:
         tc.gemm_f16_set_config(cta_group=2)
         p = tc.gemm_f16_plan(600, 520, 776, 0, num_sms=152)
-        assert (p["tile_m"], p["tiles_m"], p["tiles_n"], p["grid"], p["slots"]) == (256, 3, 3, 18, 6)
+        assert (p["tile_m"], p["tiles_m"], p["tiles_n"], p["grid"], p["slots"], p["tile_k"]) == (256, 3, 3, 18, 3, 128)
+        p = tc.gemm_f16_plan(600, 520, 200, 0, num_sms=152)       # short K keeps 64-deep steps
+        assert (p["tile_k"], p["k_steps"], p["slots"]) == (64, 4, 4)
         with pytest.raises(tc.GemmError):                       # no K steps to pair on
             tc.gemm_f16_plan(256, 256, 0, 0, num_sms=152)
         with pytest.raises(tc.GemmError):
@@ -132,6 +136,15 @@ def test_cta_pair_planning(lib):
             tc.gemm_f16_set_config(cta_group=3)
         tc.gemm_f16_set_config(cta_group=2, grid=4)
         assert tc.gemm_f16_plan(1100, 1280, 264, 0, num_sms=152)["grid"] == 4
+        # 128-deep pipeline steps: 64 KiB per step, three fit
+        tc.gemm_f16_set_config(cta_group=2, tile_k=128)
+        p = tc.gemm_f16_plan(8192, 8192, 8200, 0, num_sms=152)
+        assert (p["tile_k"], p["k_steps"], p["slots"]) == (128, 65, 3)
+        tc.gemm_f16_set_config(cta_group=1, tile_k=128)            # single-CTA kernel: 64 only
+        with pytest.raises(tc.GemmError):
+            tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152)
+        with pytest.raises(tc.GemmError):
+            tc.gemm_f16_set_config(tile_k=96)
     finally:
         tc.gemm_f16_set_config()
 
@@ -200,8 +213,8 @@ def test_stages_clamp_and_release_rule(lib):
         assert (p["stages"], p["slots"]) == (2, 2)
         p = tc.gemm_f16_plan(128, 128, 64, 0, num_sms=152)   # 1 step
         assert (p["stages"], p["slots"]) == (1, 1)
-        p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)   # CTA pairs: 32 KiB steps
-        assert (p["cta_group"], p["stages"], p["release"], p["slots"]) == (2, 6, 0, 6)
+        p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)   # CTA pairs: 64 KiB steps
+        assert (p["cta_group"], p["stages"], p["release"], p["slots"]) == (2, 3, 0, 3)
         tc.gemm_f16_set_config(cta_group=1)
         p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)   # one CTA: 48 KiB steps
         assert (p["tile_n"], p["stages"], p["release"], p["slots"]) == (256, 4, 0, 4)

@@ -110,10 +110,12 @@ def test_split_k(split, tile_n, out_dtype):
     check_full(a, b, out_dtype, f"split {split} tile_n {tile_n}")
 
 
-PAIR_VARIANTS = [dict(cta_group=2, stages=s, release=r) for s, r in [(1, 0), (2, 1), (3, 0), (4, 2), (6, 0)]]
+PAIR_VARIANTS = ([dict(cta_group=2, tile_k=64, stages=s, release=r) for s, r in [(1, 0), (2, 1), (3, 0), (4, 2), (6, 0)]]
+                 + [dict(cta_group=2, tile_k=128, stages=s, release=r) for s, r in [(1, 0), (2, 1), (3, 0)]])
 
 
-@pytest.mark.parametrize("cfg", PAIR_VARIANTS, ids=lambda c: f"pair_s{c['stages']}r{c['release']}")
+@pytest.mark.parametrize("cfg", PAIR_VARIANTS,
+                         ids=lambda c: f"pair_k{c.get('tile_k', 64)}_s{c['stages']}r{c['release']}")
 def test_cta_pair_variants(cfg):
     """256 x 256 tiles on a CTA pair (cta_group::2): ragged M (half a pair
     tile past the edge), N and K, every ring depth and release depth."""
@@ -129,9 +131,12 @@ def test_cta_pair_persistent_and_tiny():
     tc.gemm_f16_set_config(cta_group=2, grid=4, raster_group=2)
     a, b = make_inputs(1100, 1280, 264, ("normal", 1.0), ("normal", 1.0), seed_a=3, seed_b=4)
     check_full(a, b, 0, "pair persistent")
-    tc.gemm_f16_set_config(cta_group=2)
-    a, b = make_inputs(64, 72, 40, ("normal", 1.0), ("normal", 1.0), seed_a=5, seed_b=6)
-    check_full(a, b, 1, "pair tiny")
+    tc.gemm_f16_set_config(cta_group=2, tile_k=128, grid=4, raster_group=2)
+    check_full(a, b, 1, "pair persistent, 128-deep steps")
+    for tk in (64, 128):
+        tc.gemm_f16_set_config(cta_group=2, tile_k=tk)
+        a, b = make_inputs(64, 72, 40, ("normal", 1.0), ("normal", 1.0), seed_a=5, seed_b=6)
+        check_full(a, b, 1, f"pair tiny, step {tk}")
 
 
 def test_split_k_is_deterministic():
