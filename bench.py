@@ -210,10 +210,14 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def kernel_family(plan: dict) -> str:
+    return "gemm_f16_pair_kernel" if plan.get("cta_group") == 2 else "gemm_f16_kernel"
+
+
 def recorded_traffic(workload: str, plan: dict) -> int | None:
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    if it was taken on the current kernel sources; else None."""
-    path = os.path.join(ROOT, "profiles", f"gemm_f16_kernel_{workload}.md")
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_family(plan)}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
