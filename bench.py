@@ -305,7 +305,8 @@ def workload_config(w, plan) -> dict:
            "l2": "inputs rotated over 3 copies, each larger than L2 (A+B+C > 126 MB)"}
     if plan is not None:
         cfg["plan"] = {k: plan[k] for k in ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "release", "slots", "split", "grid",
-                                            "raster_group", "num_tiles", "k_steps")}
+                                            "raster_group", "num_tiles", "k_steps", "dp_tiles", "sk_tiles", "sk_pairs",
+                                            "workspace_bytes")}
     return cfg
 
 
@@ -327,13 +328,19 @@ def run_ours(args, w, dist: Dist):
     As = [a_cpu.to(dev) for _ in range(n_copies)]
     Bs = [b_cpu.to(dev) for _ in range(n_copies)]
     Cs = [torch.empty((w.M, w.N), dtype=out_t, device=dev) for _ in range(n_copies)]
-    plan = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype)
+    # stream-K workspace (zero-filled once, outside the timed region), when the
+    # plan for this problem uses one
+    ws = tc.workspace(w.M, w.N, w.K, w.out_dtype, device=dev)
+    plan = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, with_workspace=ws is not None)
     stream = torch.cuda.current_stream(dev)
     handle = stream.cuda_stream
+    ws_ptr = ws.data_ptr() if ws is not None else 0
+    ws_bytes = ws.numel() if ws is not None else 0
 
     def step(i):
         j = i % n_copies
-        rc = tc.gemm_f16(As[j].data_ptr(), Bs[j].data_ptr(), Cs[j].data_ptr(), w.M, w.N, w.K, w.out_dtype, handle)
+        rc = tc.gemm_f16_ws(As[j].data_ptr(), Bs[j].data_ptr(), Cs[j].data_ptr(), w.M, w.N, w.K, w.out_dtype,
+                            ws_ptr, ws_bytes, handle)
         if rc != 0:
             raise tc.GemmError(rc)
 
@@ -373,7 +380,7 @@ def run_ours(args, w, dist: Dist):
 
     e2e = None
     if args.e2e_steps > 0:
-        e2e = run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, As[0], Bs[0], Cs[0], out_t)
+        e2e = run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, As[0], Bs[0], Cs[0], out_t, ws)
 
     if dist.rank == 0:
         peaks, peak_src = load_peaks()
@@ -411,7 +418,7 @@ def run_ours(args, w, dist: Dist):
     return 0
 
 
-def run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, a_d, b_d, c_d, out_t):
+def run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, a_d, b_d, c_d, out_t, ws):
     """The same metric through the public API (tc.matmul) with host buffers:
     each step copies A and B in from pinned memory and C back out."""
     import torch
@@ -425,7 +432,7 @@ def run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, a_d, b_d, c_d, out_t):
     def e2e_step():
         a_d.copy_(a_h, non_blocking=True)
         b_d.copy_(b_h, non_blocking=True)
-        tc.matmul(a_d, b_d, out_dtype=out_t, out=c_d)
+        tc.matmul(a_d, b_d, out_dtype=out_t, out=c_d, workspace=ws)
         c_h.copy_(c_d, non_blocking=True)
 
     for _ in range(3):

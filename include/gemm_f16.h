@@ -29,6 +29,8 @@
 #ifndef TCGEMM_GEMM_F16_H
 #define TCGEMM_GEMM_F16_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -58,7 +60,8 @@ typedef enum {
     GEMM_ERR_LAUNCH = -8,         /* the kernel launch failed */
     GEMM_ERR_CUDA = -9,           /* no usable CUDA device or driver entry point */
     GEMM_ERR_ARCH = -10,          /* the current device is not compute capability 10.3 */
-    GEMM_ERR_DEVICE_TIMEOUT = -11 /* a kernel's bounded wait ran out (see gemm_f16_device_status) */
+    GEMM_ERR_DEVICE_TIMEOUT = -11, /* a kernel's bounded wait ran out (see gemm_f16_device_status) */
+    GEMM_ERR_WORKSPACE = -12       /* the workspace given to gemm_f16_ws is smaller than its plan needs */
 } gemm_status;
 
 /* What the planner chose for one problem (gemm_f16_plan). */
@@ -77,6 +80,10 @@ typedef struct {
     int smem_bytes;             /* dynamic shared memory per CTA */
     int tmem_cols;              /* Tensor Memory columns per CTA */
     int threads;                /* threads per CTA */
+    int dp_tiles;               /* tiles run data-parallel (all of them without stream-K) */
+    int sk_tiles;               /* tiles whose K iterations are shared by clusters (stream-K) */
+    int sk_pairs;               /* CTA-pair clusters sharing them */
+    long long workspace_bytes;  /* workspace gemm_f16_ws needs for its stream-K plan; 0 if none */
 } gemm_plan;
 
 /* Tuning override.  Zero in a field means "planner default". */
@@ -93,6 +100,9 @@ typedef struct {
                               (256 x 256 tiles; needs tile_n 0 or 256 and no split) */
     int tile_k;            /* 0 = planner default; K depth of one pipeline step: 64, or 128
                               (CTA pairs only) */
+    int stream_k;          /* 0 = planner default (gemm_f16_ws shares the last, partly
+                              filled wave of CTA-pair tiles); 1 = never; 2 = share the K
+                              iterations of every tile (testing) */
     int inject_stall;      /* test hook: 1 makes every CTA's producer issue no loads, so
                               the MMA warp's bounded wait runs out and the kernel reports
                               GEMM_ERR_DEVICE_TIMEOUT instead of finishing.  0 in normal use. */
@@ -124,6 +134,31 @@ int gemm_f16(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, in
              gemm_stream_t stream);
 
 /*
+ * As gemm_f16, with a caller-owned device workspace for stream-K.  When the
+ * tiles of the CTA-pair kernel do not fill the last wave, the K iterations of
+ * that wave's tiles are shared evenly by the pairs, whose partial tiles meet
+ * through the workspace (flags and fp32 partials).  `workspace_bytes` must be
+ * at least what gemm_f16_workspace_size reports, else GEMM_ERR_WORKSPACE.
+ *
+ *   workspace  device pointer, 256-byte aligned; zero-filled by the caller
+ *              before its FIRST use with this library (the library keeps it
+ *              valid for later calls); NULL runs exactly as gemm_f16
+ *   ownership  the caller's; it may be reused by the next call on the same
+ *              stream, but two calls that may overlap on the GPU must not
+ *              share one workspace
+ * Errors: those of gemm_f16, GEMM_ERR_ALIGN for a misaligned workspace and
+ * GEMM_ERR_WORKSPACE for a short one.
+ */
+int gemm_f16_ws(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, int K, int out_dtype,
+                void *workspace, size_t workspace_bytes, gemm_stream_t stream);
+
+/*
+ * Bytes of workspace gemm_f16_ws needs for this problem (0 when its plan
+ * uses none), for `num_sms` SMs (0: the current device).
+ */
+int gemm_f16_workspace_size(int M, int N, int K, int out_dtype, int num_sms, size_t *bytes);
+
+/*
  * The plan gemm_f16 would use for this problem under the current config.
  * num_sms > 0 plans for that many SMs without touching CUDA (host-only);
  * num_sms == 0 asks the current device.  `out` is caller-owned host memory.
@@ -131,6 +166,9 @@ int gemm_f16(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, in
  * for out == NULL, GEMM_ERR_CUDA when num_sms == 0 and no device answers.
  */
 int gemm_f16_plan(int M, int N, int K, int out_dtype, int num_sms, gemm_plan *out);
+
+/* The plan gemm_f16_ws would use given a large enough workspace. */
+int gemm_f16_plan_ws(int M, int N, int K, int out_dtype, int num_sms, gemm_plan *out);
 
 /* Replace the process-wide tuning config (copied); NULL restores defaults.
  * Not synchronised with concurrent gemm_f16 calls on other host threads.
@@ -149,7 +187,7 @@ const char *gemm_f16_strerror(int code);
  * GEMM_ERR_DEVICE_TIMEOUT.  *site (if not NULL) receives which wait gave up
  * first (1 producer/empty slot, 2 MMA/full slot, 3 MMA/free accumulator,
  * 4 epilogue/ready accumulator, 5 drain, 6 split-K partials ready, 7 split-K
- * partials read), 0 if none.  reset != 0 clears it.
+ * partials read, 8 stream-K partial flag), 0 if none.  reset != 0 clears it.
  */
 int gemm_f16_device_status(int *site, int reset);
 

@@ -27,15 +27,18 @@ STATUS = {
     0: "GEMM_OK", -1: "GEMM_ERR_NULL", -2: "GEMM_ERR_DIM", -3: "GEMM_ERR_DTYPE",
     -4: "GEMM_ERR_ALIGN", -5: "GEMM_ERR_ALIAS", -6: "GEMM_ERR_CONFIG", -7: "GEMM_ERR_TMAP",
     -8: "GEMM_ERR_LAUNCH", -9: "GEMM_ERR_CUDA", -10: "GEMM_ERR_ARCH", -11: "GEMM_ERR_DEVICE_TIMEOUT",
+    -12: "GEMM_ERR_WORKSPACE",
 }
-EXPORTED = ["gemm_f16", "gemm_f16_plan", "gemm_f16_set_config", "gemm_f16_get_config",
-            "gemm_f16_strerror", "gemm_f16_device_status", "gemm_f16_abi_version"]
+EXPORTED = ["gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_plan", "gemm_f16_plan_ws",
+            "gemm_f16_set_config", "gemm_f16_get_config", "gemm_f16_strerror", "gemm_f16_device_status",
+            "gemm_f16_abi_version"]
 
 
 class GemmPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "cta_group", "tile_m", "tile_n", "tile_k", "tiles_m", "tiles_n", "num_tiles", "k_steps", "stages",
-        "release", "slots", "split", "grid", "raster_group", "smem_bytes", "tmem_cols", "threads")]
+        "release", "slots", "split", "grid", "raster_group", "smem_bytes", "tmem_cols", "threads",
+        "dp_tiles", "sk_tiles", "sk_pairs")] + [("workspace_bytes", ctypes.c_longlong)]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -45,7 +48,7 @@ class GemmConfig(ctypes.Structure):
     _fields_ = [("tile_n", ctypes.c_int), ("stages", ctypes.c_int), ("release", ctypes.c_int),
                 ("grid", ctypes.c_int), ("raster_group", ctypes.c_int),
                 ("wait_limit", ctypes.c_longlong), ("split", ctypes.c_int), ("cta_group", ctypes.c_int), ("tile_k", ctypes.c_int),
-                ("inject_stall", ctypes.c_int)]
+                ("stream_k", ctypes.c_int), ("inject_stall", ctypes.c_int)]
 
 
 class GemmError(RuntimeError):
@@ -73,6 +76,12 @@ def load_library(path: str = LIB_PATH):
             lib.gemm_f16.restype = ci
             lib.gemm_f16_plan.argtypes = [ci, ci, ci, ci, ci, ctypes.POINTER(GemmPlan)]
             lib.gemm_f16_plan.restype = ci
+            lib.gemm_f16_plan_ws.argtypes = [ci, ci, ci, ci, ci, ctypes.POINTER(GemmPlan)]
+            lib.gemm_f16_plan_ws.restype = ci
+            lib.gemm_f16_ws.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
+            lib.gemm_f16_ws.restype = ci
+            lib.gemm_f16_workspace_size.argtypes = [ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_size_t)]
+            lib.gemm_f16_workspace_size.restype = ci
             lib.gemm_f16_set_config.argtypes = [ctypes.POINTER(GemmConfig)]
             lib.gemm_f16_set_config.restype = ci
             lib.gemm_f16_get_config.argtypes = [ctypes.POINTER(GemmConfig)]
@@ -96,12 +105,39 @@ def gemm_f16(A: int, B: int, C: int, M: int, N: int, K: int, out_dtype: int, str
     return load_library().gemm_f16(A, B, C, M, N, K, out_dtype, stream)
 
 
-def gemm_f16_plan(M: int, N: int, K: int, out_dtype: int = GEMM_OUT_F16, num_sms: int = 0) -> dict:
+def gemm_f16_ws(A: int, B: int, C: int, M: int, N: int, K: int, out_dtype: int, workspace: int,
+                workspace_bytes: int, stream: int = 0) -> int:
+    """The C entry point with a stream-K workspace (raw device pointers); returns its status."""
+    return load_library().gemm_f16_ws(A, B, C, M, N, K, out_dtype, workspace, workspace_bytes, stream)
+
+
+def gemm_f16_plan(M: int, N: int, K: int, out_dtype: int = GEMM_OUT_F16, num_sms: int = 0,
+                  with_workspace: bool = False) -> dict:
     p = GemmPlan()
-    rc = load_library().gemm_f16_plan(M, N, K, out_dtype, num_sms, ctypes.byref(p))
+    fn = load_library().gemm_f16_plan_ws if with_workspace else load_library().gemm_f16_plan
+    rc = fn(M, N, K, out_dtype, num_sms, ctypes.byref(p))
     if rc != 0:
         raise GemmError(rc, "gemm_f16_plan")
     return p.as_dict()
+
+
+def gemm_f16_workspace_size(M: int, N: int, K: int, out_dtype: int = GEMM_OUT_F16, num_sms: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    rc = load_library().gemm_f16_workspace_size(M, N, K, out_dtype, num_sms, ctypes.byref(n))
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_workspace_size")
+    return n.value
+
+
+def workspace(M: int, N: int, K: int, out_dtype=GEMM_OUT_F16, device=None):
+    """A zero-filled device workspace for gemm_f16_ws / matmul(workspace=...),
+    or None when the problem's plan needs none (torch allocates it)."""
+    import torch
+
+    nbytes = gemm_f16_workspace_size(M, N, K, _out_code(out_dtype))
+    if nbytes == 0:
+        return None
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device if device is not None else "cuda")
 
 
 def gemm_f16_set_config(**fields) -> None:
@@ -141,12 +177,14 @@ def _out_code(out_dtype) -> int:
     raise ValueError(f"out_dtype must be torch.float16 or torch.float32, got {out_dtype}")
 
 
-def matmul(a, b, out_dtype=None, out=None, stream=None):
+def matmul(a, b, out_dtype=None, out=None, stream=None, workspace=None):
     """C = a @ b for fp16 CUDA tensors a [M, K] and b [K, N]; C is fp16 (default) or fp32.
 
     The kernel is enqueued on ``stream`` (default: torch's current stream) and
-    the call returns without synchronising.  Raises ``GemmError`` on a nonzero
-    status from the library and ``ValueError`` on tensors it cannot take.
+    the call returns without synchronising.  ``workspace``: a CUDA tensor from
+    ``workspace(...)`` (zero-filled before its first use) enables stream-K.
+    Raises ``GemmError`` on a nonzero status from the library and
+    ``ValueError`` on tensors it cannot take.
     """
     import torch
 
@@ -172,7 +210,13 @@ def matmul(a, b, out_dtype=None, out=None, stream=None):
         stream = torch.cuda.current_stream(a.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     with torch.cuda.device(a.device):
-        rc = gemm_f16(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, code, handle)
+        if workspace is None:
+            rc = gemm_f16(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, code, handle)
+        else:
+            if not workspace.is_cuda:
+                raise ValueError("workspace must be a CUDA tensor")
+            rc = gemm_f16_ws(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, code, workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), handle)
     if rc != 0:
         raise GemmError(rc)
     return out

@@ -28,6 +28,7 @@ enum WaitSite : unsigned {
     kSiteDrain = 5,
     kSiteReduceReady = 6,
     kSiteReduceDone = 7,
+    kSitePartialFlag = 8,
 };
 
 __device__ unsigned int g_status;
@@ -41,6 +42,13 @@ struct KernelParams {
     int split;             // CTAs (one cluster) sharing a tile along K; 1 = no split
     long long wait_limit;  // clock cycles a single wait may take before giving up
     int inject;            // test hook: 1 = the producer issues no loads at all
+    // stream-K (CTA-pair kernel): tiles [0, dp_tiles) run data-parallel; the
+    // K iterations of the remaining sk_tiles are shared evenly by the first
+    // sk_pairs clusters, partial tiles meeting through `ws` and `flags`
+    int dp_tiles, sk_tiles, sk_pairs;
+    unsigned epoch;        // value a flag takes when its partial is ready in this launch
+    float* ws;             // sk_pairs x 2 CTAs x 128 x 256 fp32 partials
+    unsigned* flags;       // sk_pairs x 2 CTAs x 4 epilogue warps
 };
 
 template <int BN, int OUT>

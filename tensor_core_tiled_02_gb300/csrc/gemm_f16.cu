@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -28,11 +29,13 @@ struct DeviceInfo {
     bool ready = false;
     int sms = 0;
     int cc = 0;
+    int max_pairs = 0;  // CTA-pair clusters the GPU holds at once (0: not yet asked)
     bool attr_set[5][2] = {};  // [tile_n 64 / 128 / 256, CTA pair step K 64 / 128][out_dtype]
 };
 DeviceInfo g_dev[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<unsigned> g_epoch{0};  // stream-K flag value of the latest launch
 std::once_flag g_encode_once;
 
 int out_bytes(int out_dtype) { return out_dtype == GEMM_OUT_F16 ? 2 : 4; }
@@ -74,6 +77,7 @@ int check_config(const gemm_config& c) {
     if (c.cta_group < 0 || c.cta_group > 2) return GEMM_ERR_CONFIG;
     if (c.cta_group == 2 && ((c.tile_n != 0 && c.tile_n != 256) || c.split > 1)) return GEMM_ERR_CONFIG;
     if (c.tile_k != 0 && c.tile_k != 64 && c.tile_k != 128) return GEMM_ERR_CONFIG;
+    if (c.stream_k < 0 || c.stream_k > 2) return GEMM_ERR_CONFIG;
     return GEMM_OK;
 }
 
@@ -127,7 +131,16 @@ int max_slots_for_pair(int out_dtype, int step_k) {
 // emit_pipeline, stages must exceed release, and stages is clamped to the
 // steps one CTA runs (never below release + 1).  Default: the deepest ring
 // that fits shared memory.
-int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config& cfg, gemm_plan* p) {
+// Workspace of a stream-K plan: a flag per epilogue warp of every CTA of the
+// sharing clusters (rounded up to 256 bytes), then one fp32 partial tile half
+// (128 x 256) per CTA.
+size_t workspace_for(int sk_pairs) {
+    const size_t flags = ((size_t)sk_pairs * 8 * sizeof(unsigned) + 255) / 256 * 256;
+    return flags + (size_t)sk_pairs * 2 * kPartialFloats * sizeof(float);
+}
+
+int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bool with_workspace,
+              const gemm_config& cfg, gemm_plan* p) {
     std::memset(p, 0, sizeof(*p));
     p->tile_m = kBM;
     p->tile_k = kBK;
@@ -171,14 +184,52 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
         p->tiles_n = ceil_div(N, 256);
         p->num_tiles = p->tiles_m * p->tiles_n;
         p->split = 1;
-        int pairs = p->num_tiles < num_sms / 2 ? p->num_tiles : num_sms / 2;
-        if (cfg.grid > 0 && cfg.grid / 2 < pairs) pairs = cfg.grid / 2 > 0 ? cfg.grid / 2 : 1;
+        if (cfg.grid > 0 && cfg.grid / 2 < max_pairs) max_pairs = cfg.grid / 2 > 0 ? cfg.grid / 2 : 1;
+        int pairs = p->num_tiles < max_pairs ? p->num_tiles : max_pairs;
+        // Stream-K (needs a workspace): when the last wave of tiles would leave
+        // pairs idle, each of its R tiles is split along K into s equal parts,
+        // s = pairs / R (2..4, at least 8 K steps a part), run by s * R pairs at
+        // once.  Equal parts keep the pairs that hold part j of different tiles
+        // on the same K range at the same time, so tiles sharing a row block of
+        // A or a column block of B still share it in L2.  The full waves stay
+        // data-parallel.  stream_k 2 (testing) shares every tile's iterations
+        // evenly over all pairs instead.
+        p->dp_tiles = p->num_tiles;
+        int sk_tiles = 0, sk_pairs = 0, clusters = pairs;
+        if (cfg.stream_k == 2) {
+            clusters = max_pairs;
+            sk_tiles = p->num_tiles;
+            const long long iters = (long long)sk_tiles * p->k_steps;
+            sk_pairs = (int)(iters < clusters ? iters : clusters);
+        } else if (cfg.stream_k == 0) {
+            const int R = p->num_tiles < max_pairs ? p->num_tiles : p->num_tiles % pairs;
+            if (R > 0) {
+                int parts = max_pairs / R;
+                if (parts > 4) parts = 4;
+                if (parts > p->k_steps / 8) parts = p->k_steps / 8;
+                if (parts >= 2) {
+                    sk_tiles = R;
+                    sk_pairs = parts * R;
+                    clusters = p->num_tiles < max_pairs ? sk_pairs : pairs;
+                }
+            }
+        }
+        if (sk_tiles > 0) {
+            p->workspace_bytes = (long long)workspace_for(sk_pairs);
+            if (with_workspace) {
+                p->dp_tiles = p->num_tiles - sk_tiles;
+                p->sk_tiles = sk_tiles;
+                p->sk_pairs = sk_pairs;
+                pairs = clusters;
+            }
+        }
         p->grid = 2 * pairs;
         const int d = cfg.release;
         const int max_slots = max_slots_for_pair(out_dtype, sk);
         int s = cfg.stages > 0 ? cfg.stages : max_slots - d;
         if (s <= d || s + d > max_slots) return GEMM_ERR_CONFIG;
-        const long long steps_per_cta = (long long)p->k_steps * ceil_div(p->num_tiles, pairs);
+        long long steps_per_cta = (long long)p->k_steps * ceil_div(p->num_tiles, pairs);
+        if (p->sk_tiles > 0) steps_per_cta = (long long)p->k_steps * (p->dp_tiles / pairs + 2);
         if (steps_per_cta < s) s = (int)(steps_per_cta > d ? steps_per_cta : d + 1);
         p->stages = s;
         p->release = d;
@@ -190,6 +241,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const gemm_config
         return GEMM_OK;
     }
     p->cta_group = 1;
+    p->dp_tiles = p->num_tiles;
     if (cfg.tile_k != 0 && cfg.tile_k != kBK) return GEMM_ERR_CONFIG;  // deep steps: pairs only
 
     int split = cfg.split;
@@ -359,27 +411,53 @@ int launch(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, 
     return GEMM_OK;
 }
 
-}  // namespace
+// CTA-pair clusters the GPU can hold at once (stream-K owners wait on other
+// clusters, so every cluster of a launch must be resident together).
+int max_pairs_of(DeviceInfo& dev) {
+    if (dev.max_pairs == 0) {
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3(dev.sms, 1, 1);
+        lc.blockDim = dim3(kThreads, 1, 1);
+        lc.dynamicSmemBytes = kSmemLimit;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        auto kern = gemm_f16_pair_kernel<0, 128>;
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = dev.sms / 2;
+        }
+        dev.max_pairs = n < dev.sms / 2 ? n : dev.sms / 2;
+    }
+    return dev.max_pairs;
+}
 
-extern "C" {
+gemm_config current_config() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_cfg;
+}
 
-int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype,
-             gemm_stream_t stream) {
+int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype, void* workspace,
+        size_t workspace_bytes, gemm_stream_t stream) {
     int rc = check_args(A, B, C, M, N, K, out_dtype, true);
     if (rc == 1) return GEMM_OK;
     if (rc != GEMM_OK) return rc;
-    gemm_config cfg;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        cfg = g_cfg;
-    }
+    if (workspace && ((uintptr_t)workspace & 255)) return GEMM_ERR_ALIGN;
+    const gemm_config cfg = current_config();
     DeviceInfo* dev = nullptr;
     rc = device_info(&dev);
     if (rc != GEMM_OK) return rc;
     if (dev->cc != 103) return GEMM_ERR_ARCH;
     gemm_plan plan;
-    rc = plan_impl(M, N, K, out_dtype, dev->sms, cfg, &plan);
+    rc = plan_impl(M, N, K, out_dtype, dev->sms, max_pairs_of(*dev), workspace != nullptr, cfg, &plan);
     if (rc != GEMM_OK) return rc;
+    if (plan.sk_tiles > 0 && (size_t)plan.workspace_bytes > workspace_bytes) return GEMM_ERR_WORKSPACE;
 
     std::call_once(g_encode_once, init_encode);
     if (!g_encode) return GEMM_ERR_CUDA;
@@ -399,6 +477,7 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
     if (rc != GEMM_OK) return rc;
 
     KernelParams kp;
+    std::memset(&kp, 0, sizeof(kp));
     kp.M = M;
     kp.N = N;
     kp.K = K;
@@ -411,6 +490,18 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
     kp.split = plan.split;
     kp.wait_limit = cfg.wait_limit > 0 ? cfg.wait_limit : kDefaultWaitLimit;
     kp.inject = cfg.inject_stall;
+    kp.dp_tiles = plan.dp_tiles;
+    kp.sk_tiles = plan.sk_tiles;
+    kp.sk_pairs = plan.sk_pairs;
+    if (plan.sk_tiles > 0) {
+        // flags first, then the partial tiles (layout of workspace_for)
+        unsigned e = ++g_epoch;
+        if (e == 0) e = ++g_epoch;  // 0 is what a fresh (zero-filled) workspace holds
+        kp.epoch = e;
+        kp.flags = reinterpret_cast<unsigned*>(workspace);
+        const size_t flag_bytes = ((size_t)plan.sk_pairs * 8 * sizeof(unsigned) + 255) / 256 * 256;
+        kp.ws = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + flag_bytes);
+    }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (plan.cta_group == 2 && plan.tile_k == 128)
@@ -429,23 +520,52 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
                                      : launch<128, 1>(plan, ta, tb, tc, kp, s, *dev);
 }
 
-int gemm_f16_plan(int M, int N, int K, int out_dtype, int num_sms, gemm_plan* out) {
+int plan_entry(int M, int N, int K, int out_dtype, int num_sms, bool with_workspace, gemm_plan* out) {
     if (!out) return GEMM_ERR_NULL;
     int rc = check_args(nullptr, nullptr, nullptr, M, N, K, out_dtype, false);
     if (rc < 0) return rc;
     if (num_sms < 0) return GEMM_ERR_DIM;
+    int max_pairs = num_sms / 2;
     if (num_sms == 0) {
         DeviceInfo* dev = nullptr;
         rc = device_info(&dev);
         if (rc != GEMM_OK) return rc;
         num_sms = dev->sms;
+        max_pairs = max_pairs_of(*dev);
     }
-    gemm_config cfg;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        cfg = g_cfg;
-    }
-    return plan_impl(M, N, K, out_dtype, num_sms, cfg, out);
+    return plan_impl(M, N, K, out_dtype, num_sms, max_pairs, with_workspace, current_config(), out);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype,
+             gemm_stream_t stream) {
+    return run(A, B, C, M, N, K, out_dtype, nullptr, 0, stream);
+}
+
+int gemm_f16_ws(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype,
+                void* workspace, size_t workspace_bytes, gemm_stream_t stream) {
+    return run(A, B, C, M, N, K, out_dtype, workspace, workspace_bytes, stream);
+}
+
+int gemm_f16_plan(int M, int N, int K, int out_dtype, int num_sms, gemm_plan* out) {
+    return plan_entry(M, N, K, out_dtype, num_sms, false, out);
+}
+
+int gemm_f16_plan_ws(int M, int N, int K, int out_dtype, int num_sms, gemm_plan* out) {
+    return plan_entry(M, N, K, out_dtype, num_sms, true, out);
+}
+
+int gemm_f16_workspace_size(int M, int N, int K, int out_dtype, int num_sms, size_t* bytes) {
+    if (!bytes) return GEMM_ERR_NULL;
+    *bytes = 0;
+    gemm_plan plan;
+    int rc = plan_entry(M, N, K, out_dtype, num_sms, true, &plan);
+    if (rc != GEMM_OK) return rc;
+    *bytes = plan.sk_tiles > 0 ? (size_t)plan.workspace_bytes : 0;
+    return GEMM_OK;
 }
 
 int gemm_f16_set_config(const gemm_config* cfg) {
@@ -479,6 +599,7 @@ const char* gemm_f16_strerror(int code) {
         case GEMM_ERR_CUDA: return "no usable CUDA device or driver";
         case GEMM_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
         case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel's bounded device-side wait ran out";
+        case GEMM_ERR_WORKSPACE: return "the workspace is smaller than gemm_f16_workspace_size reports";
         default: return "unknown gemm_status code";
     }
 }

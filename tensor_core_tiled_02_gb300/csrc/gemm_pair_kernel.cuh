@@ -20,6 +20,19 @@
 //     single-CTA kernel does.
 // Persistent: cluster c walks pair tiles c, c + clusters, ... in the grouped
 // raster.  Programmatic dependent launch as in the single-CTA kernel.
+//
+// Stream-K (sk_tiles > 0): the full waves of tiles run as above; the K
+// iterations of the remaining tiles are split evenly over the first sk_pairs
+// clusters, so every cluster ends at about the same time.  A cluster's first
+// stream-K unit may start inside a tile: it is a contributor and parks its
+// fp32 partial (each CTA its 128 rows) in the workspace slot of this cluster,
+// then each epilogue warp releases its flag.  A unit that starts a tile but
+// does not finish it is the tile's owner: it comes last in its cluster, waits
+// (bounded) for the flags of the following clusters that hold the rest of the
+// tile, adds their partials in cluster order and stores the tile.  Owners only
+// wait on contributors and contributors wait on nobody, so there is no cycle;
+// all clusters are resident at once (the grid is capped at the clusters the
+// GPU can hold).
 #pragma once
 
 #include "gemm_common.cuh"
@@ -28,6 +41,69 @@ namespace tcgemm {
 
 constexpr int kPairBM = 256;  // tile rows per pair (MMA M)
 constexpr int kPairBN = 256;  // tile columns per pair (MMA N)
+constexpr int kPartialFloats = kBM * kPairBN;  // one CTA's fp32 partial of a pair tile
+
+// The units of work of one cluster: its data-parallel tiles, then its share
+// of the stream-K iterations.  Producer, MMA issuer and epilogue walk the same
+// sequence.
+struct UnitIter {
+    int next_dp, stride;
+    long long it, it_end;
+};
+
+__device__ __forceinline__ long long sk_begin(const KernelParams& p, int c) {
+    return (long long)p.sk_tiles * p.k_blocks * c / p.sk_pairs;
+}
+
+__device__ __forceinline__ void unit_iter_init(UnitIter& u, const KernelParams& p, int c, int clusters) {
+    u.next_dp = c;
+    u.stride = clusters;
+    if (p.sk_tiles > 0 && c < p.sk_pairs) {
+        u.it = sk_begin(p, c);
+        u.it_end = sk_begin(p, c + 1);
+    } else {
+        u.it = u.it_end = 0;
+    }
+}
+
+// Next unit: tile id and K-step range [k0, k1).  False when none is left.
+__device__ __forceinline__ bool unit_next(UnitIter& u, const KernelParams& p, int& tile, int& k0, int& k1) {
+    if (u.next_dp < p.dp_tiles) {
+        tile = u.next_dp;
+        u.next_dp += u.stride;
+        k0 = 0;
+        k1 = p.k_blocks;
+        return true;
+    }
+    if (u.it < u.it_end) {
+        const int KB = p.k_blocks;
+        const int local = (int)(u.it / KB);
+        k0 = (int)(u.it - (long long)local * KB);
+        const long long left = u.it_end - u.it;
+        k1 = left < (long long)(KB - k0) ? k0 + (int)left : KB;
+        tile = p.dp_tiles + local;
+        u.it += k1 - k0;
+        return true;
+    }
+    return false;
+}
+
+// Bounded wait until a flag holds this launch's epoch (acquire).
+__device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned epoch, volatile int* abort_flag,
+                                          long long limit) {
+    if (ptx::ld_acquire_gpu(f) == epoch) return true;
+    const long long t0 = clock64();
+    while (ptx::ld_acquire_gpu(f) != epoch) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            *abort_flag = 1;
+            record_timeout(kSitePartialFlag);
+            return false;
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
 
 // SK: K depth of one pipeline step, 64 or 128.  A deeper step issues twice
 // the MMAs per barrier wait and per commit, with the same bytes in flight.
@@ -108,9 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
-    const int num_tiles = p.tiles_m * p.tiles_n;  // in 256 x 256 pair tiles
-    const int first_tile = blockIdx.x >> 1;
-    const int tile_stride = gridDim.x >> 1;
+    const int cluster = blockIdx.x >> 1;   // this pair
+    const int clusters = gridDim.x >> 1;
     const int KB = p.k_blocks;
 
     if (warp == 0) {
@@ -120,12 +195,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
-            for (int t = first_tile; ok && t < num_tiles; t += tile_stride) {
+            UnitIter u;
+            unit_iter_init(u, p, cluster, clusters);
+            int t, k0, k1;
+            while (ok && unit_next(u, p, t, k0, k1)) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
                 const int m0 = mb * kPairBM + (int)rank * kBM;
                 const int n0 = nb * kPairBN + (int)rank * (kPairBN / 2);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -162,16 +240,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             long long it = 0;
             int tl = 0;
             bool ok = true;
-            for (int t = first_tile; ok && t < num_tiles; t += tile_stride, ++tl) {
+            UnitIter u;
+            unit_iter_init(u, p, cluster, clusters);
+            int t, k0, k1;
+            while (ok && unit_next(u, p, t, k0, k1)) {
                 const int acc = tl & 1;
                 const uint32_t aph = (tl >> 1) & 1;
+                ++tl;
                 if (!wait_bounded<true>(tempty_bar(acc), aph ^ 1u, abort_flag, p.wait_limit, kSiteMmaTmemEmpty)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kPairBN);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit, kSiteMmaFull)) {
                         ok = false;
                         break;
@@ -190,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the two 64-wide column blocks are one box apart.
                         const uint64_t ad = ad0 + (uint64_t)(((k / 4) * L::kAtomBytes + (k % 4) * (kUmmaK * 2)) >> 4);
                         const uint64_t bd = bd0 + (uint64_t)((k * (kUmmaK * 128)) >> 4);
-                        ptx::mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                        ptx::mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb != k0) || (k != 0));
                     }
                     if (it >= p.release) {
                         int rs = stage - p.release;
@@ -213,13 +295,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- epilogue (both CTAs): own 128 rows x 256 columns ----------------
         const int q = warp & 3;
         const uint32_t staging = sC + (uint32_t)(q * 2 * L::kStagingBytes);
+        const int row_in_tile = q * 32 + lane;
         int tl = 0;
         int nstore = 0;
-        for (int t = first_tile; t < num_tiles; t += tile_stride, ++tl) {
+        UnitIter u;
+        unit_iter_init(u, p, cluster, clusters);
+        int t, k0, k1;
+        while (unit_next(u, p, t, k0, k1)) {
             int mb, nb;
             tile_coords(t, p, mb, nb);
             const int acc = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
+            ++tl;
             if (KB > 0) {
                 if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane))
                     break;
@@ -227,6 +314,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int row0 = mb * kPairBM + (int)rank * kBM + q * 32;
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPairBN);
+
+            if (k0 > 0) {
+                // stream-K contributor: park this CTA's partial (its 128 rows) in the
+                // cluster's workspace slot as [column / 4][row] 16-byte groups
+                // (consecutive lanes, consecutive 16 bytes), then release the flag
+                float* slot = p.ws + (size_t)(cluster * 2 + (int)rank) * kPartialFloats;
+#pragma unroll 1
+                for (int c = 0; c < kPairBN / 32; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(trow + c * 32, v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        ptx::st_global_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), v[4 * j],
+                                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) ptx::st_release_gpu(p.flags + (cluster * 2 + (int)rank) * 4 + q, p.epoch);
+                continue;
+            }
+            // stream-K owner: the clusters after this one whose units start inside
+            // this tile hold the rest of its K range
+            int q_end = cluster + 1;
+            if (k1 < KB) {
+                const long long tile_end = (long long)(t - p.dp_tiles + 1) * KB;
+                while (q_end < p.sk_pairs && sk_begin(p, q_end) < tile_end) ++q_end;
+                bool ok = true;
+                for (int qq = cluster + 1; ok && qq < q_end; ++qq) {
+                    const unsigned* f = p.flags + (qq * 2 + (int)rank) * 4 + q;
+                    int r = 1;
+                    if (lane == 0) r = wait_flag(f, p.epoch, abort_flag, 4 * p.wait_limit);
+                    ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+                    if (ok) (void)ptx::ld_acquire_gpu(f);  // orders this lane's reads after the flag
+                }
+                if (!ok) break;
+            }
 #pragma unroll 1
             for (int c = 0; c < kPairBN / kCols; ++c) {
                 uint32_t v[kCols];
@@ -244,6 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
 #pragma unroll
                     for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
+                }
+                // stream-K owner: add the contributors' partials, in cluster order
+                for (int qq = cluster + 1; qq < q_end; ++qq) {
+                    const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
+                    uint32_t x[kCols];
+#pragma unroll
+                    for (int j = 0; j < kCols / 4; ++j)
+                        ptx::ld_global_cg_v4(slot + (size_t)(((c * (kCols / 4) + j) * kBM + row_in_tile) * 4),
+                                             x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+#pragma unroll
+                    for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                 }
                 store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * kPairBN + c * kCols, row0);
             }

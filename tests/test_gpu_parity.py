@@ -139,6 +139,67 @@ def test_cta_pair_persistent_and_tiny():
         check_full(a, b, 1, f"pair tiny, step {tk}")
 
 
+def ws_gemm(a, b, out_dtype, ws):
+    a_d, b_d = a.cuda(), b.cuda()
+    c = tc.matmul(a_d, b_d, out_dtype=torch.float16 if out_dtype == 0 else torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    return c.cpu()
+
+
+@pytest.mark.parametrize("grid", [0, 10])
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_stream_k_every_tile_shared(grid, out_dtype):
+    """stream_k 2: every tile's K iterations are shared by several pairs
+    (owner plus up to four contributors per tile), ragged M, N and K."""
+    tc.gemm_f16_set_config(cta_group=2, stream_k=2, grid=grid)
+    plan = tc.gemm_f16_plan(1100, 1280, 2056, out_dtype, with_workspace=True)
+    assert plan["sk_tiles"] == plan["num_tiles"] and plan["dp_tiles"] == 0
+    ws = tc.workspace(1100, 1280, 2056, out_dtype)
+    a, b = make_inputs(1100, 1280, 2056, ("normal", 1.0), ("normal", 1.0), seed_a=11, seed_b=12)
+    c = ws_gemm(a, b, out_dtype, ws)
+    parity.check(values(c), oracle_rows(a, b, out_dtype), 2056, out_dtype, f"stream-K all, grid {grid}")
+
+
+def test_stream_k_workspace_reuse_and_determinism():
+    """One workspace serves consecutive calls (flags carry a per-launch value);
+    repeated calls agree bit for bit."""
+    tc.gemm_f16_set_config(cta_group=2, stream_k=2)
+    ws = tc.workspace(1100, 1280, 2056, 1)
+    outs = []
+    for seed in (1, 2, 1):
+        a, b = make_inputs(1100, 1280, 2056, ("uniform", 1.0), ("uniform", 1.0), seed_a=seed, seed_b=seed + 5)
+        c = ws_gemm(a, b, 1, ws)
+        parity.check(values(c), oracle_rows(a, b, 1), 2056, 1, f"reuse seed {seed}")
+        outs.append(c)
+    assert torch.equal(outs[0].view(torch.int32), outs[2].view(torch.int32))
+
+
+def test_stream_k_all_ones_exact():
+    tc.gemm_f16_set_config(cta_group=2, stream_k=2)
+    ws = tc.workspace(512, 512, 32768, 1)
+    a = torch.ones((512, 32768), dtype=torch.float16, device="cuda")
+    b = torch.ones((32768, 512), dtype=torch.float16, device="cuda")
+    c = tc.matmul(a, b, out_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    assert bool((c == 32768).all())
+
+
+def test_stream_k_workspace_errors():
+    a = torch.ones((8192, 8192), dtype=torch.float16, device="cuda")
+    c = torch.empty((8192, 8192), dtype=torch.float16, device="cuda")
+    need = tc.gemm_f16_workspace_size(8192, 8192, 8192, 0)
+    assert need > 0
+    ws = torch.zeros(need + 256, dtype=torch.uint8, device="cuda")
+    assert tc.gemm_f16_ws(a.data_ptr(), a.data_ptr(), c.data_ptr(), 8192, 8192, 8192, 0, ws.data_ptr(), need - 1,
+                          0) == -12
+    assert tc.gemm_f16_ws(a.data_ptr(), a.data_ptr(), c.data_ptr(), 8192, 8192, 8192, 0, ws.data_ptr() + 16, need,
+                          0) == -4
+    # no workspace: runs data-parallel, as gemm_f16
+    assert tc.gemm_f16_ws(a.data_ptr(), a.data_ptr(), c.data_ptr(), 8192, 8192, 8192, 0, 0, 0, 0) == 0
+    torch.cuda.synchronize()
+    assert bool((c == 8192).all())
+
+
 def test_split_k_is_deterministic():
     tc.gemm_f16_set_config(split=4)
     a, b = make_inputs(128, 1024, 4096, ("uniform", 1.0), ("uniform", 1.0), seed_a=1, seed_b=2)
@@ -270,6 +331,38 @@ def test_workload_full_size_sampled(name):
     e = oracle.as_values(oracle.gemm_elems(a.numpy(), b.numpy(), ii, jj, w.out_dtype), w.out_dtype)
     parity.check(values(c)[ii, jj], e, w.K, w.out_dtype, f"{name} elements")
     print(name, diag)
+
+
+@pytest.mark.parametrize("name", ["gemm_4096", "gemm_8192"])
+def test_workload_full_size_stream_k(name):
+    """The full-size workloads through gemm_f16_ws, as the bench times them:
+    the thin last wave of tiles shared by all pairs through the workspace."""
+    w = WORKLOADS[name]
+    assert tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, with_workspace=True)["sk_tiles"] > 0
+    a, b = workload_inputs(w)
+    ws = tc.workspace(w.M, w.N, w.K, w.out_dtype)
+    c = ws_gemm(a, b, w.out_dtype, ws)
+    plan = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, with_workspace=True)
+    # the first, middle and last row of every stream-K tile's row block (grouped
+    # raster: groups of `raster_group` m-blocks, m-block fastest within a group)
+    def m_block(t):
+        g = plan["raster_group"]
+        per = g * plan["tiles_n"]
+        first = (t // per) * g
+        return first + (t % per) % min(plan["tiles_m"] - first, g)
+
+    rows = set(sampled_rows(w.M, n_random=4).tolist())
+    for t in range(plan["dp_tiles"], plan["num_tiles"]):
+        m0 = m_block(t) * 256
+        rows.update(r for r in (m0, m0 + 127, m0 + 128, m0 + 255) if r < w.M)
+    rows = np.array(sorted(rows), np.int64)
+    ref = oracle_rows(a, b, w.out_dtype, rows=rows)
+    parity.check(values(c)[rows], ref, w.K, w.out_dtype, f"{name} stream-K rows")
+    rng = np.random.default_rng(2)
+    ii = rng.integers(0, w.M, 2048)
+    jj = rng.integers(0, w.N, 2048)
+    e = oracle.as_values(oracle.gemm_elems(a.numpy(), b.numpy(), ii, jj, w.out_dtype), w.out_dtype)
+    parity.check(values(c)[ii, jj], e, w.K, w.out_dtype, f"{name} stream-K elements")
 
 
 def test_skinny_whole():
