@@ -61,7 +61,8 @@ typedef enum {
     GEMM_ERR_CUDA = -9,           /* no usable CUDA device or driver entry point */
     GEMM_ERR_ARCH = -10,          /* the current device is not compute capability 10.3 */
     GEMM_ERR_DEVICE_TIMEOUT = -11, /* a kernel's bounded wait ran out (see gemm_f16_device_status) */
-    GEMM_ERR_WORKSPACE = -12       /* the workspace given to gemm_f16_ws is smaller than its plan needs */
+    GEMM_ERR_WORKSPACE = -12,      /* the workspace given to gemm_f16_ws is smaller than its plan needs */
+    GEMM_ERR_SCRATCH_LIMIT = -13   /* the problem needs more scratch than gemm_f16_noalloc's fixed array */
 } gemm_status;
 
 /* What the planner chose for one problem (gemm_f16_plan). */
@@ -151,6 +152,31 @@ int gemm_f16(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, in
  */
 int gemm_f16_ws(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, int K, int out_dtype,
                 void *workspace, size_t workspace_bytes, gemm_stream_t stream);
+
+/*
+ * As gemm_f16_ws, for callers that cannot allocate device memory when they
+ * call: code running while a CUDA graph is captured (cudaMalloc is not
+ * allowed there), allocators and runtimes that must not re-enter the CUDA
+ * allocator, plugins handed only their input and output buffers.  The pages
+ * have no counterpart; this is an interface convenience of this library.
+ *
+ * The stream-K scratch lives in one fixed array of 20 MiB in device memory,
+ * which every GPU that loads this library holds until the process exits.
+ * Nothing is allocated or freed by the call.  A problem whose plan needs more
+ * scratch than that (more than about 80 CTA pairs sharing tiles) is refused
+ * with GEMM_ERR_SCRATCH_LIMIT.
+ *
+ *   - The first call on each device looks up the array's device address (a
+ *     runtime query, no allocation).  Make that first call before any stream
+ *     capture on that device.
+ *   - All calls share the one array and it keeps what the last call wrote.
+ *     Two calls whose kernels may overlap on the GPU (different streams, or
+ *     different host threads, without ordering between them) race on it and
+ *     may return wrong results; order them on one stream.
+ * Arguments, results and errors otherwise as gemm_f16.
+ */
+int gemm_f16_noalloc(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, int K, int out_dtype,
+                     gemm_stream_t stream);
 
 /*
  * Bytes of workspace gemm_f16_ws needs for this problem (0 when its plan

@@ -27,9 +27,10 @@ STATUS = {
     0: "GEMM_OK", -1: "GEMM_ERR_NULL", -2: "GEMM_ERR_DIM", -3: "GEMM_ERR_DTYPE",
     -4: "GEMM_ERR_ALIGN", -5: "GEMM_ERR_ALIAS", -6: "GEMM_ERR_CONFIG", -7: "GEMM_ERR_TMAP",
     -8: "GEMM_ERR_LAUNCH", -9: "GEMM_ERR_CUDA", -10: "GEMM_ERR_ARCH", -11: "GEMM_ERR_DEVICE_TIMEOUT",
-    -12: "GEMM_ERR_WORKSPACE",
+    -12: "GEMM_ERR_WORKSPACE", -13: "GEMM_ERR_SCRATCH_LIMIT",
 }
-EXPORTED = ["gemm_f16", "gemm_f16_ws", "gemm_f16_workspace_size", "gemm_f16_plan", "gemm_f16_plan_ws",
+EXPORTED = ["gemm_f16", "gemm_f16_ws", "gemm_f16_noalloc", "gemm_f16_workspace_size", "gemm_f16_plan",
+            "gemm_f16_plan_ws",
             "gemm_f16_set_config", "gemm_f16_get_config", "gemm_f16_strerror", "gemm_f16_device_status",
             "gemm_f16_abi_version"]
 
@@ -80,6 +81,8 @@ def load_library(path: str = LIB_PATH):
             lib.gemm_f16_plan_ws.restype = ci
             lib.gemm_f16_ws.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
             lib.gemm_f16_ws.restype = ci
+            lib.gemm_f16_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+            lib.gemm_f16_noalloc.restype = ci
             lib.gemm_f16_workspace_size.argtypes = [ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_size_t)]
             lib.gemm_f16_workspace_size.restype = ci
             lib.gemm_f16_set_config.argtypes = [ctypes.POINTER(GemmConfig)]

@@ -600,6 +600,8 @@ const char* gemm_f16_strerror(int code) {
         case GEMM_ERR_ARCH: return "the current device is not compute capability 10.3 (sm_103a)";
         case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel's bounded device-side wait ran out";
         case GEMM_ERR_WORKSPACE: return "the workspace is smaller than gemm_f16_workspace_size reports";
+        case GEMM_ERR_SCRATCH_LIMIT:
+            return "the problem needs more stream-K scratch than gemm_f16_noalloc's fixed 20 MiB array holds";
         default: return "unknown gemm_status code";
     }
 }
@@ -632,3 +634,68 @@ int gemm_f16_device_status(int* site, int reset) {
 int gemm_f16_abi_version(void) { return 1; }
 
 }  // extern "C"
+
+// ---- stream-K without any allocation ---------------------------------------------
+//
+// For callers that cannot allocate device memory at the point of the call: code
+// running while a CUDA graph is being captured, where cudaMalloc is not allowed;
+// allocators or runtimes that must not re-enter the CUDA allocator; plugins
+// that are handed only their input and output buffers.  gemm_f16_noalloc runs
+// the same plan as gemm_f16_ws, with the stream-K scratch (flags and fp32
+// partial tiles) in one fixed array in device memory instead of a workspace
+// the caller passes in.
+
+namespace {
+
+// The scratch: kNoAllocScratchBytes of device memory in every GPU that loads
+// this library, held until the process exits.  Zero at module load.  Calls
+// share it and it keeps what the last call wrote; the flags only ever hold the
+// launch epoch of an earlier call, which never matches a later call's.
+constexpr size_t kNoAllocScratchBytes = 20u << 20;  // 20 MiB: 76 CTA pairs' partials need 19.0 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device.  The array's name in
+// host code is only a host-side handle, so the address is asked of the runtime
+// once per device (with that device current) and then reused.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int gemm_f16_noalloc(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K,
+                                int out_dtype, gemm_stream_t stream) {
+    int rc = check_args(A, B, C, M, N, K, out_dtype, true);
+    if (rc == 1) return GEMM_OK;
+    if (rc != GEMM_OK) return rc;
+    DeviceInfo* dev = nullptr;
+    rc = device_info(&dev);
+    if (rc != GEMM_OK) return rc;
+    if (dev->cc != 103) return GEMM_ERR_ARCH;
+    gemm_plan plan;
+    rc = plan_impl(M, N, K, out_dtype, dev->sms, max_pairs_of(*dev), true, current_config(), &plan);
+    if (rc != GEMM_OK) return rc;
+    if (plan.sk_tiles > 0 && (size_t)plan.workspace_bytes > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != GEMM_OK) return rc;
+    return run(A, B, C, M, N, K, out_dtype, scratch, kNoAllocScratchBytes, stream);
+}
