@@ -65,6 +65,10 @@ def _bind(lib):
                                      ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
     lib.oracle_gemm_rows_decoded.restype = ctypes.c_int
     lib.oracle_gemm_rows_decoded.argtypes = lib.oracle_gemm_rows.argtypes
+    lib.oracle_gemm_acc_rows.restype = ctypes.c_int
+    lib.oracle_gemm_acc_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
     lib.oracle_gemm.restype = ctypes.c_int
     lib.oracle_gemm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
@@ -151,6 +155,34 @@ def gemm(A, B, out_dtype: int = OUT_F16, rows=None, nthreads=None, lib=None) -> 
                               out_dtype, rows.ctypes.data, rows.size, _threads(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_rows failed with {rc}")
+    return out
+
+
+def gemm_acc(A, B, Cin, out_dtype: int = OUT_F16, rows=None, nthreads=None, lib=None) -> np.ndarray:
+    """round_out(Cin + A @ B) over fp64, the sum starting from Cin, for the
+    listed rows.  ``Cin`` is [M, N] float16 (or its uint16 bits) or float32."""
+    lib = lib or load()
+    a = _u16(A)
+    b = _u16(B)
+    cin = np.asarray(Cin)
+    if cin.dtype == np.float32:
+        cin_dtype = OUT_F32
+    else:
+        cin = _u16(cin)
+        cin_dtype = OUT_F16
+    cin = np.ascontiguousarray(cin)
+    M, K = a.shape
+    N = b.shape[1]
+    if cin.shape != (M, N):
+        raise ValueError(f"Cin must be {(M, N)}, got {cin.shape}")
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = np.ascontiguousarray(np.asarray(rows, np.int64)).ravel()
+    out = np.zeros((rows.size, N), _out_np_dtype(out_dtype))
+    rc = lib.oracle_gemm_acc_rows(a.ctypes.data, b.ctypes.data, cin.ctypes.data, cin_dtype, out.ctypes.data, M, N,
+                                  K, out_dtype, rows.ctypes.data, rows.size, _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_gemm_acc_rows failed with {rc}")
     return out
 
 

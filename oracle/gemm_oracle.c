@@ -125,6 +125,8 @@ typedef struct {
     int N, K, out_dtype;
     const int64_t *rows;
     int64_t row_begin, row_end;
+    const void *Cin;    /* NULL, or the M x N values the sums start from */
+    int cin_dtype;      /* 0 = binary16 bits, 1 = binary32 */
 } row_job;
 
 static void *row_worker(void *arg)
@@ -135,7 +137,15 @@ static void *row_worker(void *arg)
     if (!acc) return (void *)1;
     for (int64_t r = job->row_begin; r < job->row_end; ++r) {
         int64_t i = job->rows[r];
-        for (int j = 0; j < N; ++j) acc[j] = 0.0;
+        if (job->Cin == NULL) {
+            for (int j = 0; j < N; ++j) acc[j] = 0.0;
+        } else if (job->cin_dtype == ORACLE_OUT_F16) {
+            const uint16_t *cin = (const uint16_t *)job->Cin + i * (int64_t)N;
+            for (int j = 0; j < N; ++j) acc[j] = oracle_f16_decode(cin[j]);
+        } else {
+            const float *cin = (const float *)job->Cin + i * (int64_t)N;
+            for (int j = 0; j < N; ++j) acc[j] = (double)cin[j];
+        }
         /* k ascending for every element of the row */
         for (int k = 0; k < K; ++k) {
             double a = oracle_f16_decode(job->A[i * (int64_t)K + k]);
@@ -193,8 +203,45 @@ int oracle_gemm_rows(const uint16_t *A, const uint16_t *B, void *C, int M, int N
  * oracle_f16_decode_array), so that a caller computing many row samples of
  * one product decodes B once.
  */
+static int gemm_rows_impl(const uint16_t *A, const double *Bd, const void *Cin, int cin_dtype, void *C,
+                          int M, int N, int K, int out_dtype, const int64_t *rows, int64_t nrows, int nthreads);
+
 int oracle_gemm_rows_decoded(const uint16_t *A, const double *Bd, void *C, int M, int N, int K,
                              int out_dtype, const int64_t *rows, int64_t nrows, int nthreads)
+{
+    return gemm_rows_impl(A, Bd, NULL, 0, C, M, N, K, out_dtype, rows, nrows, nthreads);
+}
+
+/*
+ * Accumulation into an existing output ("JAX Pallas 软件流水线 Software
+ * Pipelining 完全指南", section 7.2: a sum accumulated into the output block
+ * over the innermost grid axis, there initialised to zero on the first step;
+ * here initialised to the values the output already holds, as an output that
+ * aliases an input per section 7.1):
+ *
+ *   C_ref[i][j] = round_out( f64(Cin[i][j]) + sum_k f64(A[i][k]) * f64(B[k][j]) )
+ *
+ * The running sum starts at Cin and adds the products in ascending k.  Cin is
+ * M x N, binary16 bits (cin_dtype 0) or binary32 (1).  Otherwise as
+ * oracle_gemm_rows.
+ */
+int oracle_gemm_acc_rows(const uint16_t *A, const uint16_t *B, const void *Cin, int cin_dtype, void *C, int M,
+                         int N, int K, int out_dtype, const int64_t *rows, int64_t nrows, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
+    if (cin_dtype < 0 || cin_dtype > 1 || !Cin) return -1;
+    if (nrows == 0 || N == 0) return 0;
+    if (K > 0 && (!A || !B)) return -1;
+    double *Bd = (double *)malloc(sizeof(double) * (size_t)((int64_t)K * N > 0 ? (int64_t)K * N : 1));
+    if (!Bd) return -2;
+    if (K > 0) oracle_f16_decode_array(B, Bd, (int64_t)K * N);
+    int rc = gemm_rows_impl(A, Bd, Cin, cin_dtype, C, M, N, K, out_dtype, rows, nrows, nthreads);
+    free(Bd);
+    return rc;
+}
+
+static int gemm_rows_impl(const uint16_t *A, const double *Bd, const void *Cin, int cin_dtype, void *C,
+                          int M, int N, int K, int out_dtype, const int64_t *rows, int64_t nrows, int nthreads)
 {
     if (M < 0 || N < 0 || K < 0 || nrows < 0) return -1;
     if (out_dtype < 0 || out_dtype > 2) return -1;
@@ -220,6 +267,8 @@ int oracle_gemm_rows_decoded(const uint16_t *A, const double *Bd, void *C, int M
         jobs[t].rows = rows;
         jobs[t].row_begin = nrows * t / nthreads;
         jobs[t].row_end = nrows * (t + 1) / nthreads;
+        jobs[t].Cin = Cin;
+        jobs[t].cin_dtype = cin_dtype;
         if (pthread_create(&tids[t], NULL, row_worker, &jobs[t]) != 0) {
             rc = -2;
             break;

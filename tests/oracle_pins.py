@@ -278,6 +278,81 @@ def pin_elems_and_threads(lib):
         assert np.array_equal(e.view(np.uint8), r.view(np.uint8))
 
 
+# ---- accumulation into an existing output ---------------------------------------
+
+
+def pin_acc_zero_start_and_zero_product(lib):
+    """Starting from zero is the plain product (bit for bit); a zero product
+    returns the starting values (fp16 in, fp16 out: the same bits, with
+    -0 + 0 = +0 as IEEE addition gives)."""
+    rng = np.random.default_rng(31)
+    a = _rand_f16(rng, (29, 70), "normal")
+    b = _rand_f16(rng, (70, 41), "normal")
+    zero16 = np.zeros((29, 41), np.uint16)
+    for dt in (oracle.OUT_F16, oracle.OUT_F32, oracle.OUT_F64):
+        assert np.array_equal(oracle.gemm_acc(a, b, zero16, dt, lib=lib).view(np.uint8),
+                              oracle.gemm(a, b, dt, lib=lib).view(np.uint8))
+    cin = _rand_f16(rng, (29, 41), "wide")
+    got = oracle.gemm_acc(np.zeros((29, 70), np.uint16), b, cin, oracle.OUT_F16, lib=lib)
+    assert np.array_equal(got, np.where(cin == 0x8000, np.uint16(0), cin))
+    cin32 = rng.standard_normal((29, 41)).astype(np.float32)
+    got32 = oracle.gemm_acc(np.zeros((29, 70), np.uint16), b, cin32, oracle.OUT_F32, lib=lib)
+    assert np.array_equal(got32, cin32 + np.float32(0))
+
+
+def pin_acc_all_ones(lib):
+    """All-ones A and B from C = 3 give K + 3 exactly."""
+    for K in (64, 4096):
+        cin = np.full((3, 5), 3.0, np.float16)
+        c = oracle.gemm_acc(np.ones((3, K), np.float16), np.ones((K, 5), np.float16), cin, oracle.OUT_F32,
+                            lib=lib)
+        assert np.all(c == np.float32(K + 3))
+
+
+def pin_acc_exact(lib):
+    """Exact integer brute force with a starting value, on a subset of rows in
+    a scrambled order (so the starting value must be read from the source row,
+    not the output position)."""
+    rng = np.random.default_rng(41)
+    for (M, N, K), kind in [((9, 13, 21), "wide"), ((16, 24, 48), "uniform")]:
+        a = _rand_f16(rng, (M, K), kind)
+        b = _rand_f16(rng, (K, N), kind)
+        cin = _rand_f16(rng, (M, N), kind)
+        exact = exact_gemm_int48(a, b)
+        absprod = exact_gemm_int48(a & 0x7FFF, b & 0x7FFF)
+        from exact import f16_to_int24
+        cin48 = f16_to_int24(cin) * (1 << 24)
+        rows = np.array([M - 1, 0, M // 2, 1])
+        c64 = oracle.gemm_acc(a, b, cin, oracle.OUT_F64, rows=rows, lib=lib)
+        c16 = oracle.gemm_acc(a, b, cin, oracle.OUT_F16, rows=rows, lib=lib)
+        scale = Fraction(1, 2 ** 48)
+        for r, i in enumerate(rows):
+            for j in range(N):
+                q = (exact[i, j] + cin48[i, j]) * scale
+                bound = (K + 1) * U53 * (absprod[i, j] + abs(cin48[i, j])) * scale
+                assert abs(Fraction(float(c64[r, j])) - q) <= bound
+                want = round_rational(q, F16_FORMAT)
+                val = float(np.array([c16[r, j]], np.uint16).view(np.float16)[0])
+                ok = (val == want) if isinstance(want, float) else (np.isfinite(val) and Fraction(val) == want)
+                if not ok:
+                    assert distance_to_tie(q, F16_FORMAT) <= bound
+
+
+def pin_acc_fp32_start(lib):
+    """fp32 starting values: within the textbook bound of numpy's fp64
+    Cin + A @ B."""
+    rng = np.random.default_rng(43)
+    a = _rand_f16(rng, (40, 90), "normal")
+    b = _rand_f16(rng, (90, 33), "normal")
+    cin = (rng.standard_normal((40, 33)) * 10).astype(np.float32)
+    a64 = a.view(np.float16).astype(np.float64)
+    b64 = b.view(np.float16).astype(np.float64)
+    ref = cin.astype(np.float64) + a64 @ b64
+    bound = 2.0 * 91 * 2.0 ** -53 * (np.abs(cin.astype(np.float64)) + np.abs(a64) @ np.abs(b64)) + 1e-300
+    got = oracle.gemm_acc(a, b, cin, oracle.OUT_F64, lib=lib)
+    assert np.all(np.abs(got - ref) <= bound)
+
+
 ALL_PINS = [
     pin_decode_all_patterns,
     pin_round_f16,
@@ -290,4 +365,8 @@ ALL_PINS = [
     pin_fill_42,
     pin_iota,
     pin_elems_and_threads,
+    pin_acc_zero_start_and_zero_product,
+    pin_acc_all_ones,
+    pin_acc_exact,
+    pin_acc_fp32_start,
 ]

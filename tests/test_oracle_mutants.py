@@ -23,6 +23,10 @@ MUTANTS = [
     ("lost_carry", "e += 1;", "e += 0;"),
     ("f32_via_f16", "return (float)x;", "return (float)oracle_f16_decode(oracle_f16_round(x));"),
     ("first_row_only", "int64_t i = job->rows[r];", "int64_t i = job->rows[0];"),
+    ("start_value_ignored", "for (int j = 0; j < N; ++j) acc[j] = oracle_f16_decode(cin[j]);",
+     "for (int j = 0; j < N; ++j) acc[j] = 0.0;"),
+    ("start_value_wrong_row", "const uint16_t *cin = (const uint16_t *)job->Cin + i * (int64_t)N;",
+     "const uint16_t *cin = (const uint16_t *)job->Cin + r * (int64_t)N;"),
 ]
 
 
