@@ -135,6 +135,19 @@ int gemm_f16(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, in
              gemm_stream_t stream);
 
 /*
+ * C += A * B: the product accumulated into the values C already holds
+ * (in fp32, then rounded once to out_dtype).  This is the reduction of the
+ * "JAX Pallas 软件流水线 Software Pipelining 完全指南", section 7.2 (a sum
+ * accumulated into the output block along the innermost grid axis), started
+ * from C instead of zero, C being both an input and the output as section 7.1
+ * allows for aliased buffers.  C is read and written; it must still not
+ * overlap A or B.  K == 0 leaves C as it was.  Arguments and errors as
+ * gemm_f16.
+ */
+int gemm_f16_acc(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N, int K, int out_dtype,
+                 gemm_stream_t stream);
+
+/*
  * As gemm_f16, with a caller-owned device workspace for stream-K.  When the
  * tiles of the CTA-pair kernel do not fill the last wave, the K iterations of
  * that wave's tiles are shared evenly by the pairs, whose partial tiles meet

@@ -29,7 +29,7 @@ STATUS = {
     -8: "GEMM_ERR_LAUNCH", -9: "GEMM_ERR_CUDA", -10: "GEMM_ERR_ARCH", -11: "GEMM_ERR_DEVICE_TIMEOUT",
     -12: "GEMM_ERR_WORKSPACE", -13: "GEMM_ERR_SCRATCH_LIMIT",
 }
-EXPORTED = ["gemm_f16", "gemm_f16_ws", "gemm_f16_noalloc", "gemm_f16_workspace_size", "gemm_f16_plan",
+EXPORTED = ["gemm_f16", "gemm_f16_acc", "gemm_f16_ws", "gemm_f16_noalloc", "gemm_f16_workspace_size", "gemm_f16_plan",
             "gemm_f16_plan_ws",
             "gemm_f16_set_config", "gemm_f16_get_config", "gemm_f16_strerror", "gemm_f16_device_status",
             "gemm_f16_abi_version"]
@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH):
             lib.gemm_f16_plan_ws.restype = ci
             lib.gemm_f16_ws.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
             lib.gemm_f16_ws.restype = ci
+            lib.gemm_f16_acc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+            lib.gemm_f16_acc.restype = ci
             lib.gemm_f16_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
             lib.gemm_f16_noalloc.restype = ci
             lib.gemm_f16_workspace_size.argtypes = [ci, ci, ci, ci, ci, ctypes.POINTER(ctypes.c_size_t)]
@@ -178,6 +180,34 @@ def _out_code(out_dtype) -> int:
     if out_dtype in (torch.float32, GEMM_OUT_F32):
         return GEMM_OUT_F32
     raise ValueError(f"out_dtype must be torch.float16 or torch.float32, got {out_dtype}")
+
+
+def matmul_acc(a, b, c, stream=None):
+    """c += a @ b in place (c fp16 or fp32, [M, N], contiguous); returns c.
+
+    The library reads c's values before the call and adds the product to them
+    in fp32, rounding once to c's type.  Asynchronous on ``stream``.
+    """
+    import torch
+
+    if a.dtype != torch.float16 or b.dtype != torch.float16:
+        raise ValueError("a and b must be torch.float16")
+    if a.dim() != 2 or b.dim() != 2 or a.shape[1] != b.shape[0]:
+        raise ValueError(f"shape mismatch: {tuple(a.shape)} @ {tuple(b.shape)}")
+    if c.dtype not in (torch.float16, torch.float32) or tuple(c.shape) != (a.shape[0], b.shape[1]):
+        raise ValueError("c must be an fp16 or fp32 [M, N] tensor")
+    if not (a.is_contiguous() and b.is_contiguous() and c.is_contiguous()):
+        raise ValueError("a, b and c must be contiguous row-major")
+    if stream is None:
+        stream = torch.cuda.current_stream(a.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    code = GEMM_OUT_F16 if c.dtype == torch.float16 else GEMM_OUT_F32
+    with torch.cuda.device(a.device):
+        rc = load_library().gemm_f16_acc(a.data_ptr(), b.data_ptr(), c.data_ptr(), a.shape[0], b.shape[1],
+                                         a.shape[1], code, handle)
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_acc")
+    return c
 
 
 def matmul(a, b, out_dtype=None, out=None, stream=None, workspace=None):

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -49,6 +50,7 @@ struct KernelParams {
     unsigned epoch;        // value a flag takes when its partial is ready in this launch
     float* ws;             // sk_pairs x 2 CTAs x 128 x 256 fp32 partials
     unsigned* flags;       // sk_pairs x 2 CTAs x 4 epilogue warps
+    const void* c_in;      // accumulate into C: the values C holds before the call; NULL otherwise
 };
 
 template <int BN, int OUT>
@@ -184,6 +186,36 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 
 
 __device__ __forceinline__ void fadd_bits(uint32_t& acc, uint32_t add) {
     acc = __float_as_uint(__uint_as_float(acc) + __uint_as_float(add));
+}
+
+// Accumulating into C: add to a lane's chunk (row `row`, columns x .. x+127
+// bytes) the values C holds there before this call, in fp32.  The lane that
+// stores the chunk reads it first, so no other thread touches those elements.
+// Rows past M and 16-byte column groups past N (N % 8 == 0) are skipped.
+template <int OUT>
+__device__ __forceinline__ void add_c_in(uint32_t (&v)[OUT == 0 ? 64 : 32], const KernelParams& p, int row, int x) {
+    if (p.c_in == nullptr || row >= p.M) return;
+    constexpr int kPer16 = OUT == 0 ? 8 : 4;  // elements in 16 bytes
+    const char* base = static_cast<const char*>(p.c_in) + ((size_t)row * p.N + x) * (OUT == 0 ? 2 : 4);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (x + j * kPer16 >= p.N) break;
+        const uint4 w = *reinterpret_cast<const uint4*>(base + j * 16);
+        if constexpr (OUT == 0) {
+            const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[e]));
+                v[8 * j + 2 * e] = __float_as_uint(__uint_as_float(v[8 * j + 2 * e]) + f.x);
+                v[8 * j + 2 * e + 1] = __float_as_uint(__uint_as_float(v[8 * j + 2 * e + 1]) + f.y);
+            }
+        } else {
+            fadd_bits(v[4 * j], w.x);
+            fadd_bits(v[4 * j + 1], w.y);
+            fadd_bits(v[4 * j + 2], w.z);
+            fadd_bits(v[4 * j + 3], w.w);
+        }
+    }
 }
 
 }  // namespace tcgemm

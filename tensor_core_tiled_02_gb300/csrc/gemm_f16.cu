@@ -444,7 +444,7 @@ gemm_config current_config() {
 }
 
 int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype, void* workspace,
-        size_t workspace_bytes, gemm_stream_t stream) {
+        size_t workspace_bytes, gemm_stream_t stream, bool accumulate = false) {
     int rc = check_args(A, B, C, M, N, K, out_dtype, true);
     if (rc == 1) return GEMM_OK;
     if (rc != GEMM_OK) return rc;
@@ -493,6 +493,7 @@ int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, 
     kp.dp_tiles = plan.dp_tiles;
     kp.sk_tiles = plan.sk_tiles;
     kp.sk_pairs = plan.sk_pairs;
+    kp.c_in = accumulate ? C : nullptr;
     if (plan.sk_tiles > 0) {
         // flags first, then the partial tiles (layout of workspace_for)
         unsigned e = ++g_epoch;
@@ -548,6 +549,11 @@ int gemm_f16(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, in
 int gemm_f16_ws(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype,
                 void* workspace, size_t workspace_bytes, gemm_stream_t stream) {
     return run(A, B, C, M, N, K, out_dtype, workspace, workspace_bytes, stream);
+}
+
+int gemm_f16_acc(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype,
+                 gemm_stream_t stream) {
+    return run(A, B, C, M, N, K, out_dtype, nullptr, 0, stream, true);
 }
 
 int gemm_f16_plan(int M, int N, int K, int out_dtype, int num_sms, gemm_plan* out) {

@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                 }
+                add_c_in<OUT>(v, p, row0 + lane, nb * kPairBN + c * kCols);
                 store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * kPairBN + c * kCols, row0);
             }
         }
