@@ -69,6 +69,8 @@ def _bind(lib):
     lib.oracle_gemm_acc_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
+    lib.oracle_add_f32.restype = None
+    lib.oracle_add_f32.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64]
     lib.oracle_gemm.restype = ctypes.c_int
     lib.oracle_gemm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
@@ -184,6 +186,18 @@ def gemm_acc(A, B, Cin, out_dtype: int = OUT_F16, rows=None, nthreads=None, lib=
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_acc_rows failed with {rc}")
     return out
+
+
+def add_f32(X, Y, lib=None) -> np.ndarray:
+    """Z = X + Y, one binary32 addition per element (the blocked add's result)."""
+    lib = lib or load()
+    x = np.ascontiguousarray(np.asarray(X, np.float32))
+    y = np.ascontiguousarray(np.asarray(Y, np.float32))
+    if x.shape != y.shape:
+        raise ValueError("X and Y differ in shape")
+    z = np.empty_like(x)
+    lib.oracle_add_f32(x.ctypes.data, y.ctypes.data, z.ctypes.data, x.size)
+    return z
 
 
 class DecodedB:

@@ -321,3 +321,18 @@ int oracle_gemm_elems(const uint16_t *A, const uint16_t *B, void *out, int M, in
     }
     return 0;
 }
+
+/* ---- the pipelined blocked add ------------------------------------------------ */
+
+/*
+ * Z = X + Y elementwise in binary32 ("JAX Pallas 软件流水线 Software Pipelining
+ * 完全指南", section 6: two f32[4096, 4096] arrays added block by block, the
+ * result checked with assert_array_equal against x + y).  The blocking does
+ * not change any element, so the oracle is the plain definition: one IEEE
+ * binary32 addition per element (round to nearest even, as C's float + in the
+ * default floating-point environment).  n elements, any layout.
+ */
+void oracle_add_f32(const float *X, const float *Y, float *Z, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) Z[i] = X[i] + Y[i];
+}

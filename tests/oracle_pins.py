@@ -353,6 +353,44 @@ def pin_acc_fp32_start(lib):
     assert np.all(np.abs(got - ref) <= bound)
 
 
+# ---- the blocked add ----------------------------------------------------------
+
+
+def pin_add_ieee_cases(lib):
+    """Binary32 addition facts IEEE 754 fixes: exact small-integer sums, ties
+    to even, signed zeros, subnormals, overflow to inf, inf - inf = NaN."""
+    f = np.float32
+    cases = [  # (x, y, x + y)
+        (1.0, 2.0, 3.0),
+        (1.0, 2.0 ** -24, 1.0),                      # halfway below 1 + ulp: ties to the even 1
+        (1.0, 3 * 2.0 ** -24, 1.0 + 2.0 ** -22),     # halfway above: ties to even
+        (-0.0, -0.0, -0.0), (-0.0, 0.0, 0.0), (5.0, -5.0, 0.0),
+        (2.0 ** -149, 2.0 ** -149, 2.0 ** -148),      # subnormals add exactly
+        (2.0 ** -126, -(2.0 ** -149), 2.0 ** -126 - 2.0 ** -149),
+        (3.4028234663852886e38, 3.4028234663852886e38, np.inf),
+        (np.inf, 1.0, np.inf),
+    ]
+    x = np.array([c[0] for c in cases], f)
+    y = np.array([c[1] for c in cases], f)
+    want = np.array([c[2] for c in cases], f)
+    got = oracle.add_f32(x, y, lib=lib)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), (got, want)
+    assert np.isnan(oracle.add_f32(np.array([np.inf], f), np.array([-np.inf], f), lib=lib)).all()
+
+
+def pin_add_against_numpy(lib):
+    """Random binary32 operands over the whole exponent range, bit for bit
+    against numpy's float32 addition (another IEEE implementation), and the
+    pages' own check on their inputs' distribution: uniform [0, 1)."""
+    rng = np.random.default_rng(61)
+    x = (rng.choice([-1.0, 1.0], 200000) * np.exp2(rng.uniform(-140, 120, 200000))).astype(np.float32)
+    y = (rng.choice([-1.0, 1.0], 200000) * np.exp2(rng.uniform(-140, 120, 200000))).astype(np.float32)
+    assert np.array_equal(oracle.add_f32(x, y, lib=lib).view(np.uint32), (x + y).view(np.uint32))
+    u = rng.random((512, 512), dtype=np.float32)
+    v = rng.random((512, 512), dtype=np.float32)
+    assert np.array_equal(oracle.add_f32(u, v, lib=lib), u + v)
+
+
 ALL_PINS = [
     pin_decode_all_patterns,
     pin_round_f16,
@@ -369,4 +407,6 @@ ALL_PINS = [
     pin_acc_all_ones,
     pin_acc_exact,
     pin_acc_fp32_start,
+    pin_add_ieee_cases,
+    pin_add_against_numpy,
 ]

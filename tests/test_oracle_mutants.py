@@ -25,6 +25,8 @@ MUTANTS = [
     ("first_row_only", "int64_t i = job->rows[r];", "int64_t i = job->rows[0];"),
     ("start_value_ignored", "for (int j = 0; j < N; ++j) acc[j] = oracle_f16_decode(cin[j]);",
      "for (int j = 0; j < N; ++j) acc[j] = 0.0;"),
+    ("add_subtracts", "Z[i] = X[i] + Y[i];", "Z[i] = X[i] - Y[i];"),
+    ("add_drops_y", "Z[i] = X[i] + Y[i];", "Z[i] = X[i];"),
     ("start_value_wrong_row", "const uint16_t *cin = (const uint16_t *)job->Cin + i * (int64_t)N;",
      "const uint16_t *cin = (const uint16_t *)job->Cin + r * (int64_t)N;"),
 ]
