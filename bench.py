@@ -41,7 +41,8 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (fp16 in, fp32 acc) at 8192³; % of GB300 dense FP16 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["tensor_core_tiled_02_gb300/csrc/gemm_common.cuh", "tensor_core_tiled_02_gb300/csrc/gemm_kernel.cuh",
+KERNEL_SOURCES = ["tensor_core_tiled_02_gb300/csrc/add_kernel.cuh",
+                  "tensor_core_tiled_02_gb300/csrc/gemm_common.cuh", "tensor_core_tiled_02_gb300/csrc/gemm_kernel.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_pair_kernel.cuh", "tensor_core_tiled_02_gb300/csrc/ptx.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_f16.cu"]
 
@@ -211,6 +212,8 @@ def kernel_source_hash() -> str:
 
 
 def kernel_family(plan: dict) -> str:
+    if plan.get("kind") == "add":
+        return "add_f32_kernel"
     return "gemm_f16_pair_kernel" if plan.get("cta_group") == 2 else "gemm_f16_kernel"
 
 
@@ -269,6 +272,8 @@ def run_reference(args, w, dist: Dist):
 
     if dist.rank != 0:
         return 0
+    if w.kind == "add":
+        return run_reference_add(args, w)
     threads = os.cpu_count() or 1
     a, b = workload_inputs(w)
     dec = oracle.DecodedB(b.numpy())
@@ -293,6 +298,33 @@ def run_reference(args, w, dist: Dist):
         "config": workload_config(w, None),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference_add(args, w):
+    """Reference arm of the blocked add: the oracle, one whole addition per step."""
+    import oracle
+    from tensor_core_tiled_02_gb300.synthetic import add_inputs
+
+    x, y = add_inputs(w.M, w.N)
+    xn, yn = x.numpy(), y.numpy()
+    for _ in range(args.warmup):
+        oracle.add_f32(xn, yn)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.add_f32(xn, yn)
+    el = time.perf_counter() - t0
+    value = float(w.bytes_moved) * args.steps / el / 1e9
+    line = {
+        "metric": ADD_METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "M": w.M, "N": w.N},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"one whole {w.M}x{w.N} addition per step (one thread)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -452,6 +484,118 @@ def run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, a_d, b_d, c_d, out_t, ws):
             "d2h_bytes_per_step": c_h.numel() * c_h.element_size(), "steps": args.e2e_steps}
 
 
+ADD_METRIC = "blocked add GB/s (f32 Z = X + Y, each array moved once)"
+
+
+def run_ours_add(args, w, dist: Dist):
+    """The second workload: the pipelined blocked add, HBM-bound, in GB/s."""
+    import torch
+
+    import tensor_core_tiled_02_gb300 as tc
+    from tensor_core_tiled_02_gb300.synthetic import add_inputs
+
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    x_cpu, y_cpu = add_inputs(w.M, w.N)
+    n_copies = max(1, args.copies)
+    Xs = [x_cpu.to(dev) for _ in range(n_copies)]
+    Ys = [y_cpu.to(dev) for _ in range(n_copies)]
+    Zs = [torch.empty_like(Xs[0]) for _ in range(n_copies)]
+    stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream
+    lib = tc.load_library()
+
+    def step(i):
+        j = i % n_copies
+        rc = lib.add_matrices_f32(Xs[j].data_ptr(), Ys[j].data_ptr(), Zs[j].data_ptr(), w.M, w.N, handle)
+        if rc != 0:
+            raise tc.GemmError(rc, "add_matrices_f32")
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dist.local_rank, enabled=not args.no_clocks)
+    clocks.start()
+    dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    dist.barrier()
+    clock_summary = clocks.stop()
+    seconds = start.elapsed_time(end) / 1e3
+    rc, site = tc.gemm_f16_device_status(reset=True)
+    if rc != 0:
+        raise RuntimeError(f"device wait gave up in the timed region (site {site})")
+    t_max = dist.max(seconds, device=dev)
+    nbytes = float(w.bytes_moved)
+    value = dist.world * nbytes * args.steps / t_max / 1e9
+
+    e2e = None
+    if args.e2e_steps > 0:
+        x_h, y_h = x_cpu.pin_memory(), y_cpu.pin_memory()
+        z_h = torch.empty_like(x_cpu).pin_memory()
+
+        def e2e_step():
+            Xs[0].copy_(x_h, non_blocking=True)
+            Ys[0].copy_(y_h, non_blocking=True)
+            tc.add_matrices(Xs[0], Ys[0], out=Zs[0])
+            z_h.copy_(Zs[0], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = dist.max(e0.elapsed_time(e1) / 1e3, device=dev)
+        e2e = {"value": dist.world * nbytes * args.e2e_steps / e2e_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": 2 * x_h.numel() * 4, "d2h_bytes_per_step": z_h.numel() * 4,
+               "steps": args.e2e_steps}
+
+    if dist.rank == 0:
+        peaks, peak_src = load_peaks()
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        achieved = nbytes / (seconds / args.steps) / 1e9
+        cpu = None
+        if not args.no_cpu_baseline and dist.world == 1:
+            import oracle
+
+            xn, yn = x_cpu.numpy(), y_cpu.numpy()
+            oracle.add_f32(xn, yn)
+            reps, t0 = 0, time.perf_counter()
+            while time.perf_counter() - t0 < args.cpu_seconds:
+                oracle.add_f32(xn, yn)
+                reps += 1
+            el = time.perf_counter() - t0
+            cpu = {"value": nbytes * reps / el / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": f"{reps} whole {w.M}x{w.N} additions in {el:.1f} s (one thread)"}
+        line = {
+            "metric": ADD_METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "inputs": "X, Y ~ U[0, 1) f32, seeds 0/1",
+                       "l2": "inputs rotated over 3 copies, each 201 MB (> L2)", "tile": "32 x 256, 3-slot ring"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": recorded_traffic(w.name, {"kind": "add"}),
+                         "peak_source": f"hbm_gbs of {peak_src}", "kernel": "add_f32_kernel",
+                         "avg_launch_ms": 1e3 * seconds / args.steps},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps, "clocks": clock_summary,
+        }
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     from tensor_core_tiled_02_gb300.synthetic import WORKLOADS
@@ -460,6 +604,8 @@ def main(argv=None):
     dist = Dist()
     if args.impl == "reference":
         return run_reference(args, w, dist)
+    if w.kind == "add":
+        return run_ours_add(args, w, dist)
     return run_ours(args, w, dist)
 
 

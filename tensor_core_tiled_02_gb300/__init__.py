@@ -29,7 +29,7 @@ STATUS = {
     -8: "GEMM_ERR_LAUNCH", -9: "GEMM_ERR_CUDA", -10: "GEMM_ERR_ARCH", -11: "GEMM_ERR_DEVICE_TIMEOUT",
     -12: "GEMM_ERR_WORKSPACE", -13: "GEMM_ERR_SCRATCH_LIMIT",
 }
-EXPORTED = ["gemm_f16", "gemm_f16_acc", "gemm_f16_ws", "gemm_f16_noalloc", "gemm_f16_workspace_size", "gemm_f16_plan",
+EXPORTED = ["add_matrices_f32", "gemm_f16", "gemm_f16_acc", "gemm_f16_ws", "gemm_f16_noalloc", "gemm_f16_workspace_size", "gemm_f16_plan",
             "gemm_f16_plan_ws",
             "gemm_f16_set_config", "gemm_f16_get_config", "gemm_f16_strerror", "gemm_f16_device_status",
             "gemm_f16_abi_version"]
@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH):
             lib.gemm_f16_plan_ws.restype = ci
             lib.gemm_f16_ws.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp, ctypes.c_size_t, vp]
             lib.gemm_f16_ws.restype = ci
+            lib.add_matrices_f32.argtypes = [vp, vp, vp, ci, ci, vp]
+            lib.add_matrices_f32.restype = ci
             lib.gemm_f16_acc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
             lib.gemm_f16_acc.restype = ci
             lib.gemm_f16_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
@@ -180,6 +182,30 @@ def _out_code(out_dtype) -> int:
     if out_dtype in (torch.float32, GEMM_OUT_F32):
         return GEMM_OUT_F32
     raise ValueError(f"out_dtype must be torch.float16 or torch.float32, got {out_dtype}")
+
+
+def add_matrices(x, y, out=None, stream=None):
+    """Z = x + y for f32 CUDA tensors [M, N] (the pipelined blocked add); ``out``
+    may be x or y (in place).  Asynchronous on ``stream``."""
+    import torch
+
+    if x.dtype != torch.float32 or y.dtype != torch.float32 or x.shape != y.shape or x.dim() != 2:
+        raise ValueError("x and y must be f32 tensors of one 2-D shape")
+    if not (x.is_cuda and y.is_cuda and x.is_contiguous() and y.is_contiguous()):
+        raise ValueError("x and y must be contiguous CUDA tensors")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.dtype != torch.float32 or out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous f32 tensor of x's shape")
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(x.device):
+        rc = load_library().add_matrices_f32(x.data_ptr(), y.data_ptr(), out.data_ptr(), x.shape[0], x.shape[1],
+                                             handle)
+    if rc != 0:
+        raise GemmError(rc, "add_matrices_f32")
+    return out
 
 
 def matmul_acc(a, b, c, stream=None):

@@ -42,7 +42,8 @@ def needs_build() -> bool:
     if not os.path.exists(LIB):
         return True
     lib_t = os.path.getmtime(LIB)
-    deps = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "gemm_f16.h")]
+    deps = SOURCES + [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [
+        os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     return any(os.path.getmtime(d) > lib_t for d in deps)
 
 

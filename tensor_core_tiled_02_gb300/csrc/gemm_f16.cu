@@ -10,7 +10,9 @@
 #include <cstring>
 #include <mutex>
 
+#include "add_matrices.h"
 #include "gemm_f16.h"
+#include "add_kernel.cuh"
 #include "gemm_kernel.cuh"
 #include "gemm_pair_kernel.cuh"
 
@@ -301,14 +303,14 @@ void init_encode() {
 // 2-D row-major tensor map with a 128-byte swizzle; out-of-range elements
 // read as zero and are not written.
 int encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* ptr, uint64_t inner,
-              uint64_t outer, uint32_t box_inner, uint32_t box_outer) {
+              uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_TMAP;
 }
 
@@ -638,6 +640,72 @@ int gemm_f16_device_status(int* site, int reset) {
 }
 
 int gemm_f16_abi_version(void) { return 1; }
+
+int add_matrices_f32(const float* X, const float* Y, float* Z, int M, int N, gemm_stream_t stream) {
+    if (M < 0 || N < 0) return GEMM_ERR_DIM;
+    if (N % 4 != 0) return GEMM_ERR_ALIGN;
+    if ((long long)ceil_div(M, kAddBM) * ceil_div(N, kAddBN) > INT_MAX) return GEMM_ERR_DIM;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!X || !Y || !Z) return GEMM_ERR_NULL;
+    const uintptr_t x = (uintptr_t)X, y = (uintptr_t)Y, z = (uintptr_t)Z;
+    if ((x | y | z) & 15) return GEMM_ERR_ALIGN;
+    // Z may be X or Y itself (every element is read before it is written), but
+    // may not partly overlap either
+    const uint64_t bytes = (uint64_t)M * N * 4;
+    if (z != x && z < x + bytes && x < z + bytes) return GEMM_ERR_ALIAS;
+    if (z != y && z < y + bytes && y < z + bytes) return GEMM_ERR_ALIAS;
+    const gemm_config cfg = current_config();
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != GEMM_OK) return rc;
+    if (dev->cc != 103) return GEMM_ERR_ARCH;
+    std::call_once(g_encode_once, init_encode);
+    if (!g_encode) return GEMM_ERR_CUDA;
+    CUtensorMap tx, ty, tz;
+    rc = encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, X, (uint64_t)N, (uint64_t)M, kAddBN, kAddBM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != GEMM_OK) return rc;
+    rc = encode_2d(&ty, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Y, (uint64_t)N, (uint64_t)M, kAddBN, kAddBM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != GEMM_OK) return rc;
+    rc = encode_2d(&tz, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, Z, (uint64_t)N, (uint64_t)M, kAddBN,
+                   kAddBM / kAddWarps, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != GEMM_OK) return rc;
+    AddParams ap;
+    ap.M = M;
+    ap.N = N;
+    ap.tiles_m = ceil_div(M, kAddBM);
+    ap.tiles_n = ceil_div(N, kAddBN);
+    ap.slots = 3;  // at least 2: a slot is freed only after the next tile's store
+    ap.wait_limit = cfg.wait_limit > 0 ? cfg.wait_limit : kDefaultWaitLimit;
+    const int tiles = ap.tiles_m * ap.tiles_n;
+    static bool attr_done[kMaxDevices] = {};
+    int devno = 0;
+    cudaGetDevice(&devno);
+    const int smem = AddLayout::smem_bytes(ap.slots);
+    if (!attr_done[devno]) {
+        if (cudaFuncSetAttribute(add_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        attr_done[devno] = true;
+    }
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(tiles < dev->sms ? tiles : dev->sms, 1, 1);
+    lc.blockDim = dim3(kAddThreads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, add_f32_kernel, tx, ty, tz, ap) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
 
 }  // extern "C"
 

@@ -12,7 +12,7 @@ from tensor_core_tiled_02_gb300 import build as tcbuild
 from tensor_core_tiled_02_gb300.synthetic import WORKLOADS
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "gemm_f16.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))]
 
 # status codes, as the header defines them
 OK, NULL, DIM, DTYPE, ALIGN, ALIAS, CONFIG = 0, -1, -2, -3, -4, -5, -6
@@ -26,9 +26,13 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(gemm_f16\w*)\s*\(", text)))
+    """Every function the headers under include/ declare."""
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        text = re.sub(r"#[^\n]*", "", text)
+        names.update(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\([^;{]*\)\s*;", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(lib):
@@ -37,6 +41,16 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert lib.gemm_f16_abi_version() == 1
+
+
+def test_add_argument_errors_before_any_cuda_call(lib):
+    f = lib.add_matrices_f32
+    assert f(16, 16, 16, -1, 8, None) == DIM
+    assert f(16, 16, 16, 8, 6, None) == ALIGN           # rows of 24 bytes
+    assert f(0, 16, 32, 8, 8, None) == NULL
+    assert f(16, 24, 32, 8, 8, None) == ALIGN           # Y not 16-byte aligned
+    assert f(1 << 20, 1 << 30, (1 << 20) + 64, 8, 8, None) == ALIAS   # Z partly over X
+    assert f(0, 0, 0, 0, 8, None) == OK                  # empty
 
 
 def test_strerror_covers_every_code(lib):
@@ -83,6 +97,8 @@ def test_plan_matches_the_tiling_arithmetic(lib):
     # sequential steps of 64 (one CTA per tile) or 128 (CTA pairs) along K
     want_k_steps = {"gemm_256": 4, "gemm_4096": 32, "gemm_8192": 64, "skinny": 128, "long_k": 256}
     for name, w in WORKLOADS.items():
+        if w.kind != "gemm":
+            continue
         p = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, num_sms=152)
         assert p["k_steps"] == want_k_steps[name] == w.K // p["tile_k"]
         assert p["tile_m"] == 128 * p["cta_group"] and p["tile_k"] == 64 * p["cta_group"]
