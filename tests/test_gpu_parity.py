@@ -391,3 +391,57 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     c = tc.matmul(a_d, b_d)
     torch.cuda.synchronize()
     parity.check(values(c.cpu()), oracle_rows(a, b, 0), 256, 0, "after timeout")
+
+
+# ---- extreme sizes ------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("M,N,K,out_dtype", [(8, 1 << 20, 64, 0), (1 << 20, 136, 72, 0), (256, 264, 1 << 17, 1)],
+                         ids=["N=2^20", "M=2^20", "K=2^17"])
+def test_extreme_shapes_sampled(M, N, K, out_dtype):
+    """Very wide, very tall and very deep problems (the tile count, the raster
+    and the fp32 accumulation length at their largest here), on sampled rows
+    and scattered elements."""
+    a, b = make_inputs(M, N, K, ("uniform", 1.0), ("uniform", 1.0), seed_a=13, seed_b=14)
+    c = gpu_gemm(a, b, out_dtype)
+    rows = sampled_rows(M, n_random=6)
+    parity.check(values(c)[rows], oracle_rows(a, b, out_dtype, rows=rows), K, out_dtype, f"{M}x{N}x{K} rows")
+    rng = np.random.default_rng(3)
+    ii = rng.integers(0, M, 1024)
+    jj = rng.integers(0, N, 1024)
+    e = oracle.as_values(oracle.gemm_elems(a.numpy(), b.numpy(), ii, jj, out_dtype), out_dtype)
+    parity.check(values(c)[ii, jj], e, K, out_dtype, f"{M}x{N}x{K} elements")
+
+
+# ---- CUDA graphs ----------------------------------------------------------------------
+
+
+def test_graph_capture_and_replay():
+    """Launches of gemm_f16 and gemm_f16_ws captured in a CUDA graph and
+    replayed give the eager results bit for bit (tensor maps and launch
+    parameters are captured by value)."""
+    a1, b1 = make_inputs(512, 768, 1024, ("uniform", 1.0), ("uniform", 1.0), seed_a=1, seed_b=2)
+    a2, b2 = make_inputs(4096, 4096, 1024, ("uniform", 1.0), ("uniform", 1.0), seed_a=3, seed_b=4)
+    a1d, b1d, a2d, b2d = a1.cuda(), b1.cuda(), a2.cuda(), b2.cuda()
+    ws = tc.workspace(4096, 4096, 1024, 0)
+    c1 = torch.empty((512, 768), dtype=torch.float16, device="cuda")
+    c2 = torch.empty((4096, 4096), dtype=torch.float16, device="cuda")
+    # eager reference (also does each device's one-time set-up outside the capture)
+    tc.matmul(a1d, b1d, out=c1)
+    tc.matmul(a2d, b2d, out=c2, workspace=ws)
+    torch.cuda.synchronize()
+    e1, e2 = c1.clone(), c2.clone()
+    c1.zero_()
+    c2.zero_()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            tc.matmul(a1d, b1d, out=c1)
+            tc.matmul(a2d, b2d, out=c2, workspace=ws)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), e1.view(torch.int16))
+    assert torch.equal(c2.view(torch.int16), e2.view(torch.int16))
