@@ -330,11 +330,14 @@ def run_reference_add(args, w):
     return 0
 
 
-def workload_config(w, plan) -> dict:
+def workload_config(w, plan, copies: int | None = None) -> dict:
     cfg = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
            "out_dtype": "f16" if w.out_dtype == 0 else "f32",
-           "inputs": f"A ~ {w.a_dist[0]}({w.a_dist[1]:g}), B ~ {w.b_dist[0]}({w.b_dist[1]:g}), fp16, seeds 0/1",
-           "l2": "inputs rotated over 3 copies, each larger than L2 (A+B+C > 126 MB)"}
+           "inputs": f"A ~ {w.a_dist[0]}({w.a_dist[1]:g}), B ~ {w.b_dist[0]}({w.b_dist[1]:g}), fp16, seeds 0/1"}
+    if copies is not None:
+        per = (w.M * w.K + w.K * w.N) * 2 + w.M * w.N * (2 if w.out_dtype == 0 else 4)
+        cfg["l2"] = (f"inputs rotated over {copies} copies of A, B and C, {per / 1e6:.0f} MB each"
+                     + (" (> L2)" if per > 126e6 else " (each set fits in L2: time includes no flush)"))
     if plan is not None:
         cfg["plan"] = {k: plan[k] for k in ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "release", "slots", "split", "grid",
                                             "raster_group", "num_tiles", "k_steps", "dp_tiles", "sk_tiles", "sk_pairs",
@@ -438,7 +441,7 @@ def run_ours(args, w, dist: Dist):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": dist.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-            "config": workload_config(w, plan),
+            "config": workload_config(w, plan, n_copies),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -584,7 +587,8 @@ def run_ours_add(args, w, dist: Dist):
             "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "inputs": "X, Y ~ U[0, 1) f32, seeds 0/1",
-                       "l2": "inputs rotated over 3 copies, each 201 MB (> L2)", "tile": "32 x 256, 3-slot ring"},
+                       "l2": f"inputs rotated over {n_copies} copies of X, Y and Z, {3 * w.M * w.N * 4 / 1e6:.0f} MB each (> L2)",
+                       "tile": "32 x 256, 3-slot ring"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": recorded_traffic(w.name, {"kind": "add"}),
                          "peak_source": f"hbm_gbs of {peak_src}", "kernel": "add_f32_kernel",
