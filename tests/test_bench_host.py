@@ -100,3 +100,21 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == "gemm_256"
+
+
+def test_gemm_roofline_picks_the_binding_peak(monkeypatch):
+    import bench
+    from tensor_core_tiled_02_gb300.synthetic import WORKLOADS
+
+    monkeypatch.setattr(bench, "load_peaks", lambda: ({"hbm_gbs": 6700.0, "bf16_tflops": 1900.0,
+                                                       "bf16_tflops_sustained": 1700.0}, "measured"))
+    by = WORKLOADS
+    big = bench.gemm_roofline(by["gemm_8192"], 1e-3)
+    assert big["bound"] == "tensor" and big["unit"] == "TFLOP/s"
+    assert abs(big["achieved"] - 2 * 8192 ** 3 / 1e-3 / 1e12) < 1e-6
+    # M = 128: 17 GFLOP but 138 MB, about 9 us of tensor time against 21 us of HBM time
+    sk = bench.gemm_roofline(by["skinny"], 30e-6)
+    assert sk["bound"] == "hbm" and sk["unit"] == "GB/s"
+    nbytes = 2 * 128 * 8192 + 2 * 8192 * 8192 + 2 * 128 * 8192
+    assert abs(sk["achieved"] - nbytes / 30e-6 / 1e9) < 1e-6
+    assert abs(sk["frac"] - sk["achieved"] / 6700.0) < 1e-12 and 0 < sk["tensor_frac"] < sk["frac"]
