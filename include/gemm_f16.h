@@ -83,7 +83,7 @@ typedef struct {
     int threads;                /* threads per CTA */
     int dp_tiles;               /* tiles run data-parallel (all of them without stream-K) */
     int sk_tiles;               /* tiles whose K iterations are shared by clusters (stream-K) */
-    int sk_pairs;               /* CTA-pair clusters sharing them */
+    int sk_pairs;               /* clusters sharing them: CTA pairs, or single CTAs (cta_group 1) */
     long long workspace_bytes;  /* workspace gemm_f16_ws needs for its stream-K plan; 0 if none */
 } gemm_plan;
 
@@ -103,7 +103,8 @@ typedef struct {
                               (CTA pairs only) */
     int stream_k;          /* 0 = planner default (gemm_f16_ws shares the last, partly
                               filled wave of CTA-pair tiles); 1 = never; 2 = share the K
-                              iterations of every tile (testing) */
+                              iterations of every tile, also on single CTAs (needs a
+                              workspace) */
     int inject_stall;      /* test hook: 1 makes every CTA's producer issue no loads, so
                               the MMA warp's bounded wait runs out and the kernel reports
                               GEMM_ERR_DEVICE_TIMEOUT instead of finishing.  0 in normal use. */
@@ -225,8 +226,8 @@ const char *gemm_f16_strerror(int code);
  * library gave up on a bounded wait since the last reset: GEMM_OK or
  * GEMM_ERR_DEVICE_TIMEOUT.  *site (if not NULL) receives which wait gave up
  * first (1 producer/empty slot, 2 MMA/full slot, 3 MMA/free accumulator,
- * 4 epilogue/ready accumulator, 5 drain, 6 split-K partials ready, 7 split-K
- * partials read, 8 stream-K partial flag), 0 if none.  reset != 0 clears it.
+ * 4 epilogue/ready accumulator, 5 drain, 6 split-K partner ready, 7 split-K
+ * partials received, 8 stream-K partial flag), 0 if none.  reset != 0 clears it.
  */
 int gemm_f16_device_status(int *site, int reset);
 

@@ -28,7 +28,7 @@ enum WaitSite : unsigned {
     kSiteEpilogueTmemFull = 4,
     kSiteDrain = 5,
     kSiteReduceReady = 6,
-    kSiteReduceDone = 7,
+    kSiteReduceData = 7,
     kSitePartialFlag = 8,
 };
 
@@ -43,13 +43,14 @@ struct KernelParams {
     int split;             // CTAs (one cluster) sharing a tile along K; 1 = no split
     long long wait_limit;  // clock cycles a single wait may take before giving up
     int inject;            // test hook: 1 = the producer issues no loads at all
-    // stream-K (CTA-pair kernel): tiles [0, dp_tiles) run data-parallel; the
-    // K iterations of the remaining sk_tiles are shared evenly by the first
-    // sk_pairs clusters, partial tiles meeting through `ws` and `flags`
+    // stream-K: tiles [0, dp_tiles) run data-parallel; the K iterations of
+    // the remaining sk_tiles are shared evenly by the first sk_pairs clusters
+    // (CTA pairs, or single CTAs in the one-CTA kernel), partial tiles meeting
+    // through `ws` and `flags`
     int dp_tiles, sk_tiles, sk_pairs;
     unsigned epoch;        // value a flag takes when its partial is ready in this launch
-    float* ws;             // sk_pairs x 2 CTAs x 128 x 256 fp32 partials
-    unsigned* flags;       // sk_pairs x 2 CTAs x 4 epilogue warps
+    float* ws;             // one 128 x 256 fp32 partial per CTA of the sharing clusters
+    unsigned* flags;       // one flag per epilogue warp of those CTAs
     const void* c_in;      // accumulate into C: the values C holds before the call; NULL otherwise
 };
 
@@ -63,7 +64,7 @@ struct Layout {
     static constexpr int kStagingBytes = 32 * 128;       // one warp's 32 rows x 128 bytes
     static constexpr int kTmemCols = 2 * BN;             // two accumulators
     static constexpr int kPartialBytes = kBM * BN * 4;   // one fp32 partial tile (split-K)
-    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain, red_ready, red_done
+    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain, red_ready, red_data
     static constexpr int kNumBars = 2 * kMaxStages + 7;
     static constexpr int kFixedBytes = 4 * 2 * kStagingBytes + kNumBars * 8 + 16;
     static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
@@ -101,6 +102,73 @@ __device__ __forceinline__ void tile_coords(int t, const KernelParams& p, int& m
 }
 
 __device__ __forceinline__ void record_timeout(unsigned site) { atomicCAS(&g_status, 0u, site); }
+
+constexpr int kPartialFloats = kBM * 256;  // one CTA's fp32 partial tile (up to 128 x 256) in the workspace
+
+// The units of work of one cluster (a CTA pair, or a single CTA): its
+// data-parallel tiles c, c + clusters, ... below dp_tiles, then its share of
+// the stream-K iterations.  Producer, MMA issuer and epilogue walk the same
+// sequence.
+struct UnitIter {
+    int next_dp, stride;
+    long long it, it_end;
+};
+
+// First stream-K iteration of cluster c: the sk_tiles * k_blocks iterations
+// are dealt out in sk_pairs contiguous, equal (to one) shares.
+__device__ __forceinline__ long long sk_begin(const KernelParams& p, int c) {
+    return (long long)p.sk_tiles * p.k_blocks * c / p.sk_pairs;
+}
+
+__device__ __forceinline__ void unit_iter_init(UnitIter& u, const KernelParams& p, int c, int clusters) {
+    u.next_dp = c;
+    u.stride = clusters;
+    if (p.sk_tiles > 0 && c < p.sk_pairs) {
+        u.it = sk_begin(p, c);
+        u.it_end = sk_begin(p, c + 1);
+    } else {
+        u.it = u.it_end = 0;
+    }
+}
+
+// Next unit: tile id and K-step range [k0, k1).  False when none is left.
+__device__ __forceinline__ bool unit_next(UnitIter& u, const KernelParams& p, int& tile, int& k0, int& k1) {
+    if (u.next_dp < p.dp_tiles) {
+        tile = u.next_dp;
+        u.next_dp += u.stride;
+        k0 = 0;
+        k1 = p.k_blocks;
+        return true;
+    }
+    if (u.it < u.it_end) {
+        const int KB = p.k_blocks;
+        const int local = (int)(u.it / KB);
+        k0 = (int)(u.it - (long long)local * KB);
+        const long long left = u.it_end - u.it;
+        k1 = left < (long long)(KB - k0) ? k0 + (int)left : KB;
+        tile = p.dp_tiles + local;
+        u.it += k1 - k0;
+        return true;
+    }
+    return false;
+}
+
+// Bounded wait until a flag holds this launch's epoch (acquire).
+__device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned epoch, volatile int* abort_flag,
+                                          long long limit) {
+    if (ptx::ld_acquire_gpu(f) == epoch) return true;
+    const long long t0 = clock64();
+    while (ptx::ld_acquire_gpu(f) != epoch) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > limit) {
+            *abort_flag = 1;
+            record_timeout(kSitePartialFlag);
+            return false;
+        }
+        __nanosleep(64);
+    }
+    return true;
+}
 
 // Bounded wait on an mbarrier phase.  Gives up (returning false) when the
 // CTA-wide abort flag is raised or, after `limit` cycles, raises it itself.

@@ -22,13 +22,37 @@
 // Split-K (split > 1): a cluster of `split` CTAs owns one tile; CTA rank r
 // runs its own contiguous share of the K steps into its own TMEM, and the
 // partial sums meet through distributed shared memory.  The tile's output
-// column chunks are dealt out round-robin (chunk c belongs to rank c % split).
-// Every rank parks its fp32 partial of the chunks it does not own in its (now
-// idle) ring buffers and arrives on the other ranks' `red_ready` barriers;
-// each rank then adds, for the chunks it owns, the other ranks' partials to
-// its own in ascending rank order (deterministic), drains them as above, and arrives on the others'
-// `red_done`, which keeps every rank's shared memory alive until it is read.
-// The planner gives each cluster exactly one tile in this mode.
+// column chunks are dealt out round-robin (chunk c belongs to rank c % split);
+// a rank's partial of a chunk it does not own travels as one contiguous block
+// per epilogue warp ([column / 4][row] 16-byte groups) into a ring buffer.
+//   split = 2 (push): once its MMAs are done, each rank stores its partial of
+//     the other's chunks straight from TMEM through registers into the other
+//     CTA (st.async, counted as bytes on the other's `red_data` barrier).  The
+//     blocks land in the receiving warp's output staging buffers, idle until
+//     that warp drains, so a rank pushes as soon as its own MMAs are done and
+//     the transfer overlaps the other rank's last steps.  When a warp's blocks
+//     outgrow its staging (128 x 256 tiles), they land in the other's ring
+//     instead, once the other reports it idle (`red_ready`).
+//   split > 2 (pull): each rank parks the chunks it does not own in its own
+//     ring, arrives on the others' `red_ready`, and reads the other ranks'
+//     blocks of its own chunks over distributed shared memory.
+// An owner adds the other ranks' partials to its own in ascending rank order
+// (deterministic) and drains the sum as above.  A cluster barrier, arrived at
+// as soon as a thread is done with the other CTAs and waited on just before
+// leaving, keeps every rank's shared memory and barriers alive while the
+// others may still touch them.  The planner gives each cluster exactly one
+// tile in this mode.
+//
+// Stream-K (split = 1, sk_tiles > 0): as in the CTA-pair kernel, the K
+// iterations of the shared tiles are dealt out in equal contiguous shares to
+// sk_pairs CTAs, so every SM streams about the same number of K steps.  A
+// CTA's first unit may start inside a tile: it is a contributor and parks its
+// fp32 partial in its workspace slot, then each epilogue warp releases its
+// flag.  A unit that starts a tile without finishing it is the tile's owner;
+// it is its CTA's last unit, waits (bounded) for the flags of the following
+// CTAs that hold the rest of the tile, and adds their partials in CTA order
+// before storing.  Owners wait only on contributors, which wait on nobody;
+// the grid never exceeds the CTAs the GPU holds at once.
 //
 // Programmatic dependent launch: the prologue (barriers, TMEM, tensor-map
 // prefetch) runs before `griddepcontrol.wait`, so it overlaps the tail of the
@@ -70,12 +94,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kMaxStages + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
     const uint32_t red_ready_bar = bar0 + 8u * (2 * kMaxStages + 5);
-    const uint32_t red_done_bar = bar0 + 8u * (2 * kMaxStages + 6);
+    const uint32_t red_data_bar = bar0 + 8u * (2 * kMaxStages + 6);
+    // split-K parking: chunk c, epilogue warp quadrant q -> one contiguous
+    // block of kCols / 4 column groups x 32 rows x 16 bytes in the ring
+    constexpr int kChunks = BN / kCols;
+    constexpr uint32_t kWarpChunkBytes = kCols / 4 * 32 * 16;
+    auto park_at = [&](int c, int qd) { return sA + (uint32_t)(c * 4 + qd) * kWarpChunkBytes; };
+    // split 2: the blocks a warp receives (its share of at most ceil(chunks / 2)
+    // chunks) fit its two staging buffers for tiles up to 128 columns
+    constexpr bool kPushToStaging = (kChunks + 1) / 2 * kWarpChunkBytes <= 2 * L::kStagingBytes;
+    auto push_slot = [&](int c, int qd) {  // where chunk c's block of warp qd lands in its owner
+        return kPushToStaging ? sC + (uint32_t)(qd * 2 * L::kStagingBytes) + (uint32_t)(c / 2) * kWarpChunkBytes
+                              : park_at(c, qd);
+    };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int split = p.split;
     const uint32_t rank = split > 1 ? ptx::cluster_ctarank() : 0u;
+    // split-K: the chunks this rank owns
+    const int owned = (int)rank < kChunks ? (kChunks - (int)rank + split - 1) / split : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -87,9 +125,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(tempty_bar(a), 4);  // one arrive per epilogue warp
         }
         ptx::mbar_init(drain_bar, 1);
-        // split-K: the 4 epilogue warps of every other rank arrive on these
+        // split-K: the 4 epilogue warps of every other rank arrive on red_ready;
+        // red_data (split 2): this CTA's own expect-tx arrival plus the pushed bytes
         ptx::mbar_init(red_ready_bar, split > 1 ? 4 * (split - 1) : 1);
-        ptx::mbar_init(red_done_bar, split > 1 ? 4 * (split - 1) : 1);
+        ptx::mbar_init(red_data_bar, 1);
+        // split 2: armed now for every byte the partner will push here
+        if (split == 2 && owned > 0) ptx::mbar_arrive_expect_tx(red_data_bar, (uint32_t)owned * 4u * kWarpChunkBytes);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -112,27 +153,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::grid_dependency_wait();
     ptx::grid_launch_dependents();
 
-    const int num_tiles = p.tiles_m * p.tiles_n;
-    const int first_tile = blockIdx.x / split;
-    const int tile_stride = gridDim.x / split;
-    // this CTA's share of the K steps (all of them without split-K)
+    // this CTA's cluster (itself without split-K) and the clusters of the grid
+    const int cl = blockIdx.x / split;
+    const int clusters = gridDim.x / split;
+    // split-K: this rank's share of every tile's K steps, and the chunks it owns
     const int kb_begin = (int)((long long)p.k_blocks * rank / split);
     const int kb_end = (int)((long long)p.k_blocks * (rank + 1) / split);
-    const int KB = kb_end - kb_begin;
+    const bool has_k = p.k_blocks > 0;
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         // (with the test hook set, nothing is loaded: the MMA warp's first wait
         // must run out and the whole CTA must wind down through the abort path)
-        if (lane == 0 && KB > 0 && p.inject == 0) {
+        if (lane == 0 && has_k && p.inject == 0) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;  // per slot: ever issued, parity of last issue
             bool ok = true;
-            for (int t = first_tile; ok && t < num_tiles; t += tile_stride) {
+            UnitIter u;
+            unit_iter_init(u, p, cl, clusters);
+            int t, k0, k1;
+            while (ok && unit_next(u, p, t, k0, k1)) {
+                if (split > 1) k0 = kb_begin, k1 = kb_end;
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
-                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -157,25 +202,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S; ++s)
                 if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_phase >> s) & 1u, p.wait_limit);
         }
+        // split-K: the producer never touches another CTA
+        if (split > 1) ptx::cluster_arrive();
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0 && KB > 0) {
+        if (lane == 0 && has_k) {
             constexpr uint32_t idesc = make_idesc(kBM, BN);
             int stage = 0;
             uint32_t phase = 0;
             long long it = 0;
             int tl = 0;
             bool ok = true;
-            for (int t = first_tile; ok && t < num_tiles; t += tile_stride, ++tl) {
+            UnitIter u;
+            unit_iter_init(u, p, cl, clusters);
+            int t, k0, k1;
+            while (ok && unit_next(u, p, t, k0, k1)) {
+                if (split > 1) k0 = kb_begin, k1 = kb_end;
                 const int acc = tl & 1;
                 const uint32_t aph = (tl >> 1) & 1;
+                ++tl;
                 if (!wait_bounded(tempty_bar(acc), aph ^ 1u, abort_flag, p.wait_limit, kSiteMmaTmemEmpty)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit, kSiteMmaFull)) {
                         ok = false;
                         break;
@@ -190,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // consecutive 64-wide N blocks are one 8 KiB box apart.
                         const uint64_t ad = sw128_desc(a0 + k * (kUmmaK * 2), 16, 1024);
                         const uint64_t bd = sw128_desc(b0 + k * (kUmmaK * 128), kBoxBytes, 1024);
-                        ptx::mma_f16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0);
+                        ptx::mma_f16_ss(d_tmem, ad, bd, idesc, (kb != k0) || (k != 0));
                     }
                     // release the slot `release` steps back once these MMAs are done
                     if (it >= p.release) {
@@ -211,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(drain_bar);
             wait_drain(drain_bar, 0, p.wait_limit);
         }
+        if (split > 1) ptx::cluster_arrive();
     } else {
         // ---------------- epilogue: TMEM -> registers -> SMEM -> TMA store ----------------
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
@@ -218,12 +271,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row_in_tile = q * 32 + lane;
         int tl = 0;
         int nstore = 0;
-        for (int t = first_tile; t < num_tiles; t += tile_stride, ++tl) {
+        bool arrived = false;
+        UnitIter u;
+        unit_iter_init(u, p, cl, clusters);
+        int t, k0, k1;
+        while (unit_next(u, p, t, k0, k1)) {
+            if (split > 1) k0 = kb_begin, k1 = kb_end;
             int mb, nb;
             tile_coords(t, p, mb, nb);
             const int acc = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
-            if (KB > 0) {
+            ++tl;
+            if (has_k) {
                 // a legitimate wait here spans a whole tile's main loop: allow 4x
                 if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane))
                     break;
@@ -232,27 +291,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = mb * kBM + q * 32;
             const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 
-            if (split > 1) {
-                // park the partial of every chunk another rank owns, laid out as
-                // [column / 4][row] 16-byte groups so consecutive lanes touch
-                // consecutive 16 bytes (no bank conflicts, here or in the remote reads)
+            if (split == 2) {
+                const uint32_t peer = rank ^ 1u;
+                if constexpr (!kPushToStaging) {
+                    // this CTA's MMAs are done, so its ring is idle: the partner may push
+                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, peer));
+                    if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane))
+                        break;
+                }
+                // this warp's rows of the partner's chunks: TMEM -> registers -> the
+                // partner (consecutive lanes, consecutive 16 bytes)
 #pragma unroll 1
-                for (int c = 0; c < BN / kCols; ++c) {
+                for (int c = 0; c < kChunks; ++c) {
+                    if (c % 2 == (int)rank) continue;
+#pragma unroll 1
+                    for (int h = 0; h < kCols / 32; ++h) {
+                        uint32_t v[32];
+                        ptx::tmem_ld_32x32b_x32(trow + c * kCols + h * 32, v);
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            ptx::st_async_v4(ptx::mapa(push_slot(c, q) + (uint32_t)(((h * 8 + j) * 32 + lane) * 16), peer),
+                                             v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
+                                             ptx::mapa(red_data_bar, peer));
+                    }
+                }
+                // the partner's blocks of this CTA's chunks
+                if (owned > 0 &&
+                    !warp_wait<true>(red_data_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceData, lane))
+                    break;
+                // done with the partner: its pushes have landed here, and it arrives
+                // only once this CTA's pushes have landed there
+                ptx::cluster_arrive();
+                arrived = true;
+            } else if (split > 2) {
+                // park the partial of every chunk another rank owns in this CTA's
+                // ring: this warp's 32 rows as [column / 4][row] 16-byte groups
+#pragma unroll 1
+                for (int c = 0; c < kChunks; ++c) {
                     if (c % split == (int)rank) continue;
 #pragma unroll 1
                     for (int h = 0; h < kCols / 32; ++h) {
                         uint32_t v[32];
-                        const int col = c * kCols + h * 32;
-                        if (KB > 0) {
-                            ptx::tmem_ld_32x32b_x32(trow + col, v);
-                            ptx::tmem_ld_wait();
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = 0u;
-                        }
+                        ptx::tmem_ld_32x32b_x32(trow + c * kCols + h * 32, v);
+                        ptx::tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            ptx::st_shared_v4(sA + (uint32_t)(((col / 4 + j) * kBM + row_in_tile) * 16), v[4 * j],
+                            ptx::st_shared_v4(park_at(c, q) + (uint32_t)(((h * 8 + j) * 32 + lane) * 16), v[4 * j],
                                               v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
                 }
@@ -261,13 +346,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int r = 0; r < split; ++r)
                         if (r != (int)rank) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, (uint32_t)r));
                 if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane)) break;
+            } else if (k0 > 0) {
+                // stream-K contributor: park this CTA's partial in its workspace
+                // slot as [column / 4][row] 16-byte groups (consecutive lanes,
+                // consecutive 16 bytes), then release this warp's flag
+                float* slot = p.ws + (size_t)cl * kPartialFloats;
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t v[32];
+                    ptx::tmem_ld_32x32b_x32(trow + c * 32, v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        ptx::st_global_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), v[4 * j],
+                                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) ptx::st_release_gpu(p.flags + cl * 4 + q, p.epoch);
+                continue;
+            }
+            // stream-K owner: the CTAs after this one whose shares start inside
+            // this tile hold the rest of its K range
+            int q_end = cl + 1;
+            if (split == 1 && k1 < p.k_blocks) {
+                const long long tile_end = (long long)(t - p.dp_tiles + 1) * p.k_blocks;
+                while (q_end < p.sk_pairs && sk_begin(p, q_end) < tile_end) ++q_end;
+                bool ok = true;
+                for (int qq = cl + 1; ok && qq < q_end; ++qq) {
+                    const unsigned* f = p.flags + qq * 4 + q;
+                    int r = 1;
+                    if (lane == 0) r = wait_flag(f, p.epoch, abort_flag, 4 * p.wait_limit);
+                    ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+                    if (ok) (void)ptx::ld_acquire_gpu(f);  // orders this lane's reads after the flag
+                }
+                if (!ok) break;
             }
 
 #pragma unroll 1
             for (int c = 0; c < BN / kCols; ++c) {
                 if (split > 1 && c % split != (int)rank) continue;
                 uint32_t v[kCols];
-                if (KB > 0) {
+                if (has_k) {
                     ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                     if constexpr (OUT == 0)
                         ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
@@ -282,7 +405,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
                 }
-                if (split > 1) {
+                if (split == 2) {
+                    // the partner's partial, pushed into this CTA
+                    uint32_t x[kCols];
+#pragma unroll
+                    for (int j = 0; j < kCols / 4; ++j)
+                        ptx::ld_shared_v4(push_slot(c, q) + (uint32_t)((j * 32 + lane) * 16), x[4 * j], x[4 * j + 1],
+                                          x[4 * j + 2], x[4 * j + 3]);
+                    // every lane has its values before any lane reuses the staging
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
+                } else if (split > 2) {
                     // add the other ranks' partials to this rank's own, in ascending
                     // rank order: a fixed order, so the result is deterministic
                     for (int r = 0; r < split; ++r) {
@@ -290,36 +424,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // all of the chunk's remote loads in flight at once, then the adds
                         uint32_t x[kCols];
 #pragma unroll
-                        for (int j = 0; j < kCols / 4; ++j) {
-                            const int g = c * (kCols / 4) + j;  // 16-byte column group
-                            ptx::ld_cluster_v4(ptx::mapa(sA + (uint32_t)((g * kBM + row_in_tile) * 16), (uint32_t)r),
+                        for (int j = 0; j < kCols / 4; ++j)
+                            ptx::ld_cluster_v4(ptx::mapa(park_at(c, q) + (uint32_t)((j * 32 + lane) * 16), (uint32_t)r),
                                                x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-                        }
 #pragma unroll
                         for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                     }
                 }
+                // stream-K owner: add the contributors' partials, in CTA order
+                for (int qq = cl + 1; qq < q_end; ++qq) {
+                    const float* slot = p.ws + (size_t)qq * kPartialFloats;
+                    uint32_t x[kCols];
+#pragma unroll
+                    for (int j = 0; j < kCols / 4; ++j)
+                        ptx::ld_global_cg_v4(slot + (size_t)(((c * (kCols / 4) + j) * kBM + row_in_tile) * 4),
+                                             x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+#pragma unroll
+                    for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
+                }
                 add_c_in<OUT>(v, p, row0 + lane, nb * BN + c * kCols);
                 store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, row0);
             }
-            if (split > 1) {
-                // this rank has read every partial it needs; wait until the others
-                // have read this rank's before its shared memory may go away
-                __syncwarp();
-                if (lane == 0)
-                    for (int r = 0; r < split; ++r)
-                        if (r != (int)rank) ptx::mbar_arrive_cluster(ptx::mapa(red_done_bar, (uint32_t)r));
-                warp_wait(red_done_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceDone, lane);
-            }
         }
+        // after an abort: bytes the partner may still push land before this CTA leaves
+        if (split == 2 && owned > 0 && warp == 2 && lane == 0) wait_drain(red_data_bar, 0, p.wait_limit);
         // the staging buffers must have been read before shared memory goes
         // away; the global writes themselves complete with the grid
         if (lane == 0) ptx::bulk_wait_group_read<0>();
         __syncwarp();
+        if (split > 1 && !arrived) ptx::cluster_arrive();
     }
 
     ptx::tc_fence_before();
     __syncthreads();
+    // split-K: no rank leaves while another may still read or write its
+    // shared memory or arrive on its barriers
+    if (split > 1) ptx::cluster_wait();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();

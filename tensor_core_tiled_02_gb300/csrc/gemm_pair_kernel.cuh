@@ -41,69 +41,7 @@ namespace tcgemm {
 
 constexpr int kPairBM = 256;  // tile rows per pair (MMA M)
 constexpr int kPairBN = 256;  // tile columns per pair (MMA N)
-constexpr int kPartialFloats = kBM * kPairBN;  // one CTA's fp32 partial of a pair tile
-
-// The units of work of one cluster: its data-parallel tiles, then its share
-// of the stream-K iterations.  Producer, MMA issuer and epilogue walk the same
-// sequence.
-struct UnitIter {
-    int next_dp, stride;
-    long long it, it_end;
-};
-
-__device__ __forceinline__ long long sk_begin(const KernelParams& p, int c) {
-    return (long long)p.sk_tiles * p.k_blocks * c / p.sk_pairs;
-}
-
-__device__ __forceinline__ void unit_iter_init(UnitIter& u, const KernelParams& p, int c, int clusters) {
-    u.next_dp = c;
-    u.stride = clusters;
-    if (p.sk_tiles > 0 && c < p.sk_pairs) {
-        u.it = sk_begin(p, c);
-        u.it_end = sk_begin(p, c + 1);
-    } else {
-        u.it = u.it_end = 0;
-    }
-}
-
-// Next unit: tile id and K-step range [k0, k1).  False when none is left.
-__device__ __forceinline__ bool unit_next(UnitIter& u, const KernelParams& p, int& tile, int& k0, int& k1) {
-    if (u.next_dp < p.dp_tiles) {
-        tile = u.next_dp;
-        u.next_dp += u.stride;
-        k0 = 0;
-        k1 = p.k_blocks;
-        return true;
-    }
-    if (u.it < u.it_end) {
-        const int KB = p.k_blocks;
-        const int local = (int)(u.it / KB);
-        k0 = (int)(u.it - (long long)local * KB);
-        const long long left = u.it_end - u.it;
-        k1 = left < (long long)(KB - k0) ? k0 + (int)left : KB;
-        tile = p.dp_tiles + local;
-        u.it += k1 - k0;
-        return true;
-    }
-    return false;
-}
-
-// Bounded wait until a flag holds this launch's epoch (acquire).
-__device__ __forceinline__ bool wait_flag(const unsigned* f, unsigned epoch, volatile int* abort_flag,
-                                          long long limit) {
-    if (ptx::ld_acquire_gpu(f) == epoch) return true;
-    const long long t0 = clock64();
-    while (ptx::ld_acquire_gpu(f) != epoch) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > limit) {
-            *abort_flag = 1;
-            record_timeout(kSitePartialFlag);
-            return false;
-        }
-        __nanosleep(64);
-    }
-    return true;
-}
+static_assert(kPartialFloats == kBM * kPairBN, "one CTA's partial of a pair tile");
 
 // SK: K depth of one pipeline step, 64 or 128.  A deeper step issues twice
 // the MMAs per barrier wait and per commit, with the same bytes in flight.

@@ -95,6 +95,25 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for a thread that is done with the other
+// CTAs long before it may leave: arrive (release) early, wait (acquire) late.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
+// 16 bytes from registers into another CTA's shared memory; the bytes count as
+// transactions on that CTA's mbarrier (both addresses from mapa).
+__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar_cluster) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     cluster_addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(a), "=r"(b), "=r"(c), "=r"(d) : "r"(addr));
+}
+
 __device__ __forceinline__ void ld_cluster_v4(uint32_t cluster_addr, uint32_t& a, uint32_t& b, uint32_t& c,
                                               uint32_t& d) {
     // volatile keeps it after the barrier wait that publishes the data; no

@@ -276,3 +276,4 @@ def test_config_roundtrip(lib):
 def test_plan_null_out(lib):
     assert lib.gemm_f16_plan(128, 128, 64, 0, 152, None) == NULL
     assert lib.gemm_f16_get_config(None) == NULL
+

@@ -98,13 +98,16 @@ def test_persistent_many_tiles_per_cta(tile_n):
     check_full(a, b, 0, f"persistent tile_n={tile_n}")
 
 
-SPLITS = [(2, 128, 0), (2, 256, 1), (3, 128, 0), (4, 128, 1), (8, 128, 0), (5, 256, 0), (2, 64, 0), (3, 64, 1)]
+SPLITS = [(2, 128, 0), (2, 128, 1), (2, 256, 1), (3, 128, 0), (4, 128, 1), (8, 128, 0), (5, 256, 0), (2, 64, 0),
+          (2, 64, 1), (3, 64, 1)]
 
 
 @pytest.mark.parametrize("split,tile_n,out_dtype", SPLITS)
 def test_split_k(split, tile_n, out_dtype):
     """Split-K through a cluster: K steps shared unevenly (47 steps), ragged
-    M, N and K, partials summed in rank 0 through distributed shared memory."""
+    M, N and K; partials meet through distributed shared memory, pushed by
+    bulk copy between two ranks, pulled by the owner for more (with BN = 64
+    and fp16 out, one rank of a pair owns no chunk at all)."""
     tc.gemm_f16_set_config(split=split, tile_n=tile_n)
     a, b = make_inputs(200, 520, 2984, ("normal", 1.0), ("normal", 1.0), seed_a=split, seed_b=tile_n)
     check_full(a, b, out_dtype, f"split {split} tile_n {tile_n}")
@@ -158,6 +161,55 @@ def test_stream_k_every_tile_shared(grid, out_dtype):
     a, b = make_inputs(1100, 1280, 2056, ("normal", 1.0), ("normal", 1.0), seed_a=11, seed_b=12)
     c = ws_gemm(a, b, out_dtype, ws)
     parity.check(values(c), oracle_rows(a, b, out_dtype), 2056, out_dtype, f"stream-K all, grid {grid}")
+
+
+@pytest.mark.parametrize("tile_n", [64, 128, 256])
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_stream_k_one_cta_every_tile_shared(tile_n, out_dtype):
+    """stream_k 2 on the one-CTA kernel: every tile's K iterations are dealt out
+    to contiguous CTA shares (owner plus contributors through the workspace),
+    several rows of tiles in the grouped raster, ragged M, N and K."""
+    tc.gemm_f16_set_config(cta_group=1, stream_k=2, tile_n=tile_n)
+    plan = tc.gemm_f16_plan(700, 1096, 3000, out_dtype, with_workspace=True)
+    assert plan["cta_group"] == 1 and plan["sk_tiles"] == plan["num_tiles"] and plan["grid"] == plan["sk_pairs"]
+    ws = tc.workspace(700, 1096, 3000, out_dtype)
+    a, b = make_inputs(700, 1096, 3000, ("normal", 1.0), ("normal", 1.0), seed_a=21, seed_b=22)
+    c = ws_gemm(a, b, out_dtype, ws)
+    parity.check(values(c), oracle_rows(a, b, out_dtype), 3000, out_dtype, f"one-CTA stream-K, BN {tile_n}")
+
+
+@pytest.mark.parametrize("M,N,K,out_dtype", [(100, 5000, 3000, 1), (1, 8, 1024, 0), (128, 256, 65536, 0),
+                                             (77, 2056, 8200, 0)])
+def test_stream_k_one_row_of_tiles(M, N, K, out_dtype):
+    """One-CTA stream-K on a single row of tiles (ragged; up to 64 CTAs
+    sharing one tile, a single share)."""
+    tc.gemm_f16_set_config(cta_group=1, stream_k=2)
+    plan = tc.gemm_f16_plan(M, N, K, out_dtype, with_workspace=True)
+    assert plan["sk_tiles"] == plan["num_tiles"]
+    ws = tc.workspace(M, N, K, out_dtype)
+    a, b = make_inputs(M, N, K, ("uniform", 1.0), ("uniform", 1.0), seed_a=31, seed_b=32)
+    c = ws_gemm(a, b, out_dtype, ws)
+    parity.check(values(c), oracle_rows(a, b, out_dtype), K, out_dtype, f"{M}x{N}x{K} plan {plan['sk_pairs']}")
+
+
+def test_stream_k_one_cta_reuse_determinism_and_exact_sums():
+    """Consecutive calls on one workspace; repeated calls agree bit for bit;
+    all-ones sums are exact through the partials."""
+    tc.gemm_f16_set_config(cta_group=1, stream_k=2)
+    ws = tc.workspace(128, 4096, 16384, 1)
+    assert tc.gemm_f16_plan(128, 4096, 16384, 1, with_workspace=True)["sk_tiles"] > 0
+    outs = []
+    for seed in (1, 2, 1):
+        a, b = make_inputs(128, 4096, 16384, ("uniform", 1.0), ("uniform", 1.0), seed_a=seed, seed_b=seed + 5)
+        c = ws_gemm(a, b, 1, ws)
+        parity.check(values(c), oracle_rows(a, b, 1), 16384, 1, f"one-CTA reuse seed {seed}")
+        outs.append(c)
+    assert torch.equal(outs[0].view(torch.int32), outs[2].view(torch.int32))
+    a = torch.ones((128, 16384), dtype=torch.float16, device="cuda")
+    b = torch.ones((16384, 4096), dtype=torch.float16, device="cuda")
+    c = tc.matmul(a, b, out_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    assert bool((c == 16384).all())
 
 
 def test_stream_k_workspace_reuse_and_determinism():
@@ -366,10 +418,21 @@ def test_workload_full_size_stream_k(name):
 
 
 def test_skinny_whole():
-    """The memory-bound workload is small enough for the oracle to check whole."""
+    """The memory-bound workload is small enough for the oracle to check whole:
+    through gemm_f16_ws as the bench times it (split-K clusters of two, partials
+    pushed between the pair), and with one-CTA stream-K over every SM."""
     w = WORKLOADS["skinny"]
     a, b = workload_inputs(w)
-    check_full(a, b, w.out_dtype, "skinny whole")
+    plan = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, with_workspace=True)
+    assert plan["split"] == 2 and plan["sk_tiles"] == 0
+    ws = tc.workspace(w.M, w.N, w.K, w.out_dtype)
+    c = ws_gemm(a, b, w.out_dtype, ws)
+    ref = oracle_rows(a, b, w.out_dtype)
+    parity.check(values(c), ref, w.K, w.out_dtype, "skinny whole, split-K")
+    tc.gemm_f16_set_config(cta_group=1, stream_k=2)
+    ws = tc.workspace(w.M, w.N, w.K, w.out_dtype)
+    c = ws_gemm(a, b, w.out_dtype, ws)
+    parity.check(values(c), ref, w.K, w.out_dtype, "skinny whole, stream-K")
 
 
 # ---- the device-side timeout path ----------------------------------------------------

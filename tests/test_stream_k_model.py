@@ -1,5 +1,5 @@
-"""The stream-K schedule of the CTA-pair kernel, replayed on the CPU for the
-plans the planner makes.
+"""The stream-K schedule of both GEMM kernels (CTA pairs, and single CTAs),
+replayed on the CPU for the plans the planner makes.
 
 Mirrors the kernel's unit walk (data-parallel tiles c, c + clusters, ... below
 dp_tiles, then cluster c's even share [S c / P, S (c+1) / P) of the
@@ -36,7 +36,7 @@ def units_of(plan, c, clusters):
 
 
 def check_plan(plan):
-    clusters = plan["grid"] // 2
+    clusters = plan["grid"] // plan["cta_group"]
     KB = plan["k_steps"]
     cover = {}
     per_tile = {}
@@ -78,53 +78,66 @@ SHAPES = [(8192, 8192, 8192, 0), (4096, 4096, 4096, 0), (2048, 2048, 32768, 1), 
           (4096, 256, 65536, 0), (20480, 20480, 1024, 0), (600, 520, 776, 0)]
 
 
+SHAPES_ONE_ROW = [(128, 8192, 8192, 0), (128, 32768, 8192, 0), (100, 5000, 3000, 1), (64, 1000, 4096, 0),
+                  (128, 256, 65536, 1), (1, 8, 1024, 0)]
+
+
+def check_workspace(plan):
+    if plan["sk_tiles"]:
+        ctas = plan["sk_pairs"] * plan["cta_group"]
+        flags = -(-ctas * 4 * 4 // 256) * 256
+        assert plan["workspace_bytes"] == flags + ctas * 128 * 256 * 4
+
+
 @pytest.mark.parametrize("M,N,K,dt", SHAPES)
 @pytest.mark.parametrize("mode", [0, 2])
-def test_stream_k_schedule(M, N, K, dt, mode):
+@pytest.mark.parametrize("cg", [1, 2])
+def test_stream_k_schedule(M, N, K, dt, mode, cg):
     try:
-        tc.gemm_f16_set_config(cta_group=2, stream_k=mode)
+        tc.gemm_f16_set_config(cta_group=cg, stream_k=mode)
         for sms in (152, 148, 132):
             plan = tc.gemm_f16_plan(M, N, K, dt, num_sms=sms, with_workspace=True)
+            assert plan["cta_group"] == cg
+            if mode == 2:
+                assert plan["sk_tiles"] > 0
             check_plan(plan)
-            if plan["sk_tiles"]:
-                flags = -(-plan["sk_pairs"] * 8 * 4 // 256) * 256
-                assert plan["workspace_bytes"] == flags + plan["sk_pairs"] * 2 * 128 * 256 * 4
+            check_workspace(plan)
     finally:
         tc.gemm_f16_set_config()
 
 
-def test_planner_uses_stream_k_where_the_last_wave_is_thin():
-    # 36 tail tiles of 1024, two equal K halves each, on 72 of the 76 pairs
-    p = tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152, with_workspace=True)
-    assert (p["dp_tiles"], p["sk_tiles"], p["sk_pairs"], p["grid"]) == (988, 36, 72, 152)
-    p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152, with_workspace=True)
-    assert (p["dp_tiles"], p["sk_tiles"], p["sk_pairs"]) == (228, 28, 56)
-    # equal parts: pairs holding part j of different tail tiles run the same K range
-    KB = p["k_steps"]
-    S = p["sk_tiles"] * KB
-    for c in range(p["sk_pairs"]):
-        assert S * c // p["sk_pairs"] % KB == (c % 2) * KB // 2
-    # 64 tiles on 76 pairs cannot be split evenly: data-parallel
-    p = tc.gemm_f16_plan(2048, 2048, 32768, 1, num_sms=152, with_workspace=True)
-    assert (p["dp_tiles"], p["sk_tiles"], p["grid"]) == (64, 0, 128)
-    # 24 pair tiles on 76 pairs: three parts each on 72 pairs
+@pytest.mark.parametrize("M,N,K,dt", SHAPES_ONE_ROW)
+def test_stream_k_schedule_one_cta(M, N, K, dt):
     try:
-        tc.gemm_f16_set_config(cta_group=2)
-        p = tc.gemm_f16_plan(2048, 768, 8192, 0, num_sms=152, with_workspace=True)
-        assert (p["num_tiles"], p["dp_tiles"], p["sk_tiles"], p["sk_pairs"], p["grid"]) == (24, 0, 24, 72, 144)
+        tc.gemm_f16_set_config(cta_group=1, stream_k=2)
+        for sms in (152, 148, 132):
+            plan = tc.gemm_f16_plan(M, N, K, dt, num_sms=sms, with_workspace=True)
+            assert plan["cta_group"] == 1
+            check_plan(plan)
+            check_workspace(plan)
+            assert plan["split"] == 1 and plan["dp_tiles"] == 0 and plan["grid"] == plan["sk_pairs"] <= sms
+            # every share holds at least 16 K steps (or there is one share)
+            assert plan["sk_pairs"] == 1 or plan["sk_tiles"] * plan["k_steps"] // plan["sk_pairs"] >= 16
     finally:
         tc.gemm_f16_set_config()
-    # a full last wave needs no stream-K: 76 x 2 tiles
-    assert tc.gemm_f16_plan(256 * 38, 256 * 4, 4096, 0, num_sms=152, with_workspace=True)["sk_tiles"] == 0
-    # tiny problems stay data-parallel (fewer than 8 iterations per sharing pair)
-    assert tc.gemm_f16_plan(600, 520, 776, 0, num_sms=152, with_workspace=True)["sk_tiles"] == 0
+
+
+def test_one_cta_stream_k_is_opt_in():
+    # M = 128: split-K clusters of two by default, with or without a workspace
+    for ws in (False, True):
+        p = tc.gemm_f16_plan(128, 8192, 8192, 0, num_sms=152, with_workspace=ws)
+        assert (p["cta_group"], p["tile_n"], p["split"], p["sk_tiles"], p["grid"]) == (1, 128, 2, 0, 128)
     try:
-        tc.gemm_f16_set_config(stream_k=1)
-        assert tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152, with_workspace=True)["sk_tiles"] == 0
-        with pytest.raises(tc.GemmError):
-            tc.gemm_f16_set_config(stream_k=3)
+        tc.gemm_f16_set_config(cta_group=1, stream_k=2)
+        p = tc.gemm_f16_plan(128, 8192, 8192, 0, num_sms=152, with_workspace=True)
+        assert (p["split"], p["dp_tiles"], p["sk_tiles"], p["sk_pairs"], p["grid"]) == (1, 0, 64, 152, 152)
+        assert p["workspace_bytes"] == 2560 + 152 * 128 * 256 * 4
+        assert tc.gemm_f16_workspace_size(128, 8192, 8192, 0, num_sms=152) == p["workspace_bytes"]
+        # without a workspace the knob has nothing to work with
+        p = tc.gemm_f16_plan(128, 8192, 8192, 0, num_sms=152, with_workspace=False)
+        assert p["sk_tiles"] == 0 and p["workspace_bytes"] > 0
+        # an explicit split keeps the clusters
+        tc.gemm_f16_set_config(cta_group=1, stream_k=2, split=2)
+        assert tc.gemm_f16_plan(128, 8192, 8192, 0, num_sms=152, with_workspace=True)["sk_tiles"] == 0
     finally:
         tc.gemm_f16_set_config()
-    p = tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152, with_workspace=True)
-    assert tc.gemm_f16_workspace_size(8192, 8192, 8192, 0, num_sms=152) == p["workspace_bytes"] > 0
-    assert tc.gemm_f16_workspace_size(600, 520, 776, 0, num_sms=152) == 0
