@@ -7,9 +7,11 @@ product; ``--workload`` picks another of the five shapes.
 Prints ONE JSON line (rank 0):
   value      TFLOP/s = 2MNK x ranks / (max over ranks of the timed seconds / steps),
              inputs resident in HBM, rotated over 3 copies (each > L2)
-  e2e        the same metric through the public API with host buffers: the
-             H2D copy of A and B from pinned memory and the D2H copy of C are
-             inside the timed region
+  e2e        the same metric through the public API with host buffers: every
+             step's H2D copy of A and B from pinned memory and D2H copy of C
+             are inside the timed region; value: copies and GEMMs pipelined
+             over three streams and two buffer sets; serial_value: all of it
+             on one stream, in turn
   roofline   the GEMM kernel's achieved TFLOP/s (algorithmic flops / average
              launch time from CUDA events) against the measured dense peak
   cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
@@ -437,7 +439,7 @@ def run_ours(args, w, dist: Dist):
 
     e2e = None
     if args.e2e_steps > 0:
-        e2e = run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, As[0], Bs[0], Cs[0], out_t, ws)
+        e2e = run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, out_t, ws)
 
     if dist.rank == 0:
         roofline = gemm_roofline(w, avg_launch_s)
@@ -467,38 +469,100 @@ def run_ours(args, w, dist: Dist):
     return 0
 
 
-def run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, a_d, b_d, c_d, out_t, ws):
+def time_e2e(dev, steps: int, h_in, d_sets, h_outs, compute):
+    """Seconds for `steps` end-to-end steps, each copying its inputs `h_in`
+    (pinned) into a device buffer set, computing, and copying the result back
+    to a pinned host buffer.  Two ways, both timed with events on the device:
+      serial     one stream: H2D, compute, D2H, step after step;
+      pipelined  three streams and two buffer sets: step i+1's H2D overlaps
+                 step i's compute and step i-1's D2H (the streaming pattern a
+                 user would write); a set is refilled only once the compute
+                 that read it is done, and recomputed only once its result
+                 has been copied out.
+    d_sets: two lists [inputs..., output]; h_outs: two pinned host outputs.
+    Returns (serial_s, pipelined_s)."""
+    import torch
+
+    cur = torch.cuda.current_stream(dev)
+    s_in, s_c, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+
+    def serial(n):
+        ins, out = d_sets[0][:-1], d_sets[0][-1]
+        for _ in range(n):
+            for d, h in zip(ins, h_in):
+                d.copy_(h, non_blocking=True)
+            compute(ins, out, cur)
+            h_outs[0].copy_(out, non_blocking=True)
+
+    def pipelined(n):
+        for st in (s_in, s_c, s_out):
+            st.wait_stream(cur)
+        done_c, done_out = [None, None], [None, None]
+        for i in range(n):
+            k = i % 2
+            ins, out = d_sets[k][:-1], d_sets[k][-1]
+            with torch.cuda.stream(s_in):
+                if done_c[k] is not None:
+                    s_in.wait_event(done_c[k])
+                for d, h in zip(ins, h_in):
+                    d.copy_(h, non_blocking=True)
+                e_in = torch.cuda.Event()
+                e_in.record(s_in)
+            with torch.cuda.stream(s_c):
+                s_c.wait_event(e_in)
+                if done_out[k] is not None:
+                    s_c.wait_event(done_out[k])
+                compute(ins, out, s_c)
+                done_c[k] = torch.cuda.Event()
+                done_c[k].record(s_c)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done_c[k])
+                h_outs[k].copy_(out, non_blocking=True)
+                done_out[k] = torch.cuda.Event()
+                done_out[k].record(s_out)
+        for st in (s_in, s_c, s_out):
+            cur.wait_stream(st)
+
+    result = []
+    for fn in (serial, pipelined):
+        fn(3)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        fn(steps)
+        e1.record(cur)
+        torch.cuda.synchronize(dev)
+        result.append(e0.elapsed_time(e1) / 1e3)
+    return result[0], result[1]
+
+
+E2E_PIPELINE = "H2D, compute and D2H on three streams over two buffer sets; serial_value: one stream, in turn"
+
+
+def run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, out_t, ws):
     """The same metric through the public API (tc.matmul) with host buffers:
     each step copies A and B in from pinned memory and C back out."""
     import torch
 
     import tensor_core_tiled_02_gb300 as tc
 
-    a_h = a_cpu.pin_memory()
-    b_h = b_cpu.pin_memory()
-    c_h = torch.empty((w.M, w.N), dtype=out_t).pin_memory()
+    h_in = [a_cpu.pin_memory(), b_cpu.pin_memory()]
+    h_outs = [torch.empty((w.M, w.N), dtype=out_t).pin_memory() for _ in range(2)]
+    d_sets = [[torch.empty_like(a_cpu, device=dev), torch.empty_like(b_cpu, device=dev),
+               torch.empty((w.M, w.N), dtype=out_t, device=dev)] for _ in range(2)]
 
-    def e2e_step():
-        a_d.copy_(a_h, non_blocking=True)
-        b_d.copy_(b_h, non_blocking=True)
-        tc.matmul(a_d, b_d, out_dtype=out_t, out=c_d, workspace=ws)
-        c_h.copy_(c_d, non_blocking=True)
+    def compute(ins, out, st):
+        tc.matmul(ins[0], ins[1], out_dtype=out_t, out=out, workspace=ws, stream=st)
 
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(dev)
     dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_s = dist.max(e0.elapsed_time(e1) / 1e3, device=dev)
-    value = dist.world * float(w.flops) * args.e2e_steps / e2e_s / 1e12
-    return {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": (a_h.numel() + b_h.numel()) * 2,
-            "d2h_bytes_per_step": c_h.numel() * c_h.element_size(), "steps": args.e2e_steps}
+    serial_s, pipe_s = time_e2e(dev, args.e2e_steps, h_in, d_sets, h_outs, compute)
+    serial_s, pipe_s = dist.max(serial_s, device=dev), dist.max(pipe_s, device=dev)
+    work = dist.world * float(w.flops) * args.e2e_steps
+    return {"value": work / pipe_s / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in h_in),
+            "d2h_bytes_per_step": h_outs[0].numel() * h_outs[0].element_size(), "steps": args.e2e_steps,
+            "pipeline": E2E_PIPELINE, "serial_value": work / serial_s / 1e12}
 
 
 ADD_METRIC = "blocked add GB/s (f32 Z = X + Y, each array moved once)"
@@ -555,29 +619,20 @@ def run_ours_add(args, w, dist: Dist):
 
     e2e = None
     if args.e2e_steps > 0:
-        x_h, y_h = x_cpu.pin_memory(), y_cpu.pin_memory()
-        z_h = torch.empty_like(x_cpu).pin_memory()
+        h_in = [x_cpu.pin_memory(), y_cpu.pin_memory()]
+        h_outs = [torch.empty_like(x_cpu).pin_memory() for _ in range(2)]
+        d_sets = [[torch.empty_like(x_cpu, device=dev) for _ in range(3)] for _ in range(2)]
 
-        def e2e_step():
-            Xs[0].copy_(x_h, non_blocking=True)
-            Ys[0].copy_(y_h, non_blocking=True)
-            tc.add_matrices(Xs[0], Ys[0], out=Zs[0])
-            z_h.copy_(Zs[0], non_blocking=True)
+        def compute(ins, out, st):
+            tc.add_matrices(ins[0], ins[1], out=out, stream=st)
 
-        for _ in range(3):
-            e2e_step()
-        torch.cuda.synchronize(dev)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_s = dist.max(e0.elapsed_time(e1) / 1e3, device=dev)
-        e2e = {"value": dist.world * nbytes * args.e2e_steps / e2e_s / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": 2 * x_h.numel() * 4, "d2h_bytes_per_step": z_h.numel() * 4,
-               "steps": args.e2e_steps}
+        dist.barrier()
+        serial_s, pipe_s = time_e2e(dev, args.e2e_steps, h_in, d_sets, h_outs, compute)
+        serial_s, pipe_s = dist.max(serial_s, device=dev), dist.max(pipe_s, device=dev)
+        work = dist.world * nbytes * args.e2e_steps
+        e2e = {"value": work / pipe_s / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": 2 * x_cpu.numel() * 4, "d2h_bytes_per_step": x_cpu.numel() * 4,
+               "steps": args.e2e_steps, "pipeline": E2E_PIPELINE, "serial_value": work / serial_s / 1e9}
 
     if dist.rank == 0:
         peaks, peak_src = load_peaks()
