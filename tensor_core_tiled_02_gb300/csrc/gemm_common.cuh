@@ -105,10 +105,13 @@ __device__ __forceinline__ void record_timeout(unsigned site) { atomicCAS(&g_sta
 
 constexpr int kPartialFloats = kBM * 256;  // one CTA's fp32 partial tile (up to 128 x 256) in the workspace
 
-// The units of work of one cluster (a CTA pair, or a single CTA): its
-// data-parallel tiles c, c + clusters, ... below dp_tiles, then its share of
-// the stream-K iterations.  Producer, MMA issuer and epilogue walk the same
-// sequence.
+// The units of work of one cluster (a CTA pair, or a single CTA): its share
+// of the stream-K iterations first, then its data-parallel tiles c,
+// c + clusters, ... below dp_tiles.  Running the shares first keeps every
+// sharing cluster on the same K range at the same time, and an owner unit's
+// wait for its contributors' partials, and their reduction, overlap the
+// cluster's next tile instead of ending the launch.  Producer, MMA issuer and
+// epilogue walk the same sequence.
 struct UnitIter {
     int next_dp, stride;
     long long it, it_end;
@@ -131,23 +134,27 @@ __device__ __forceinline__ void unit_iter_init(UnitIter& u, const KernelParams& 
     }
 }
 
+__device__ __forceinline__ void sk_unit(UnitIter& u, const KernelParams& p, int& tile, int& k0, int& k1) {
+    const int KB = p.k_blocks;
+    const int local = (int)(u.it / KB);
+    k0 = (int)(u.it - (long long)local * KB);
+    const long long left = u.it_end - u.it;
+    k1 = left < (long long)(KB - k0) ? k0 + (int)left : KB;
+    tile = p.dp_tiles + local;
+    u.it += k1 - k0;
+}
+
 // Next unit: tile id and K-step range [k0, k1).  False when none is left.
 __device__ __forceinline__ bool unit_next(UnitIter& u, const KernelParams& p, int& tile, int& k0, int& k1) {
+    if (u.it < u.it_end) {
+        sk_unit(u, p, tile, k0, k1);
+        return true;
+    }
     if (u.next_dp < p.dp_tiles) {
         tile = u.next_dp;
         u.next_dp += u.stride;
         k0 = 0;
         k1 = p.k_blocks;
-        return true;
-    }
-    if (u.it < u.it_end) {
-        const int KB = p.k_blocks;
-        const int local = (int)(u.it / KB);
-        k0 = (int)(u.it - (long long)local * KB);
-        const long long left = u.it_end - u.it;
-        k1 = left < (long long)(KB - k0) ? k0 + (int)left : KB;
-        tile = p.dp_tiles + local;
-        u.it += k1 - k0;
         return true;
     }
     return false;

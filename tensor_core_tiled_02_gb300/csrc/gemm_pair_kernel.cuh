@@ -21,18 +21,21 @@
 // Persistent: cluster c walks pair tiles c, c + clusters, ... in the grouped
 // raster.  Programmatic dependent launch as in the single-CTA kernel.
 //
-// Stream-K (sk_tiles > 0): the full waves of tiles run as above; the K
-// iterations of the remaining tiles are split evenly over the first sk_pairs
-// clusters, so every cluster ends at about the same time.  A cluster's first
-// stream-K unit may start inside a tile: it is a contributor and parks its
-// fp32 partial (each CTA its 128 rows) in the workspace slot of this cluster,
-// then each epilogue warp releases its flag.  A unit that starts a tile but
-// does not finish it is the tile's owner: it comes last in its cluster, waits
+// Stream-K (sk_tiles > 0): the K iterations of the tiles beyond the full
+// waves are split evenly over the first sk_pairs clusters, which run their
+// shares before their data-parallel tiles, so every cluster ends at about the
+// same time.  A share that starts inside a tile is a contributor: it parks
+// its fp32 partial (each CTA its 128 rows) in the workspace slot of this
+// cluster, then each epilogue warp releases its flag.  A unit that starts a
+// tile but does not finish it is the tile's owner: its epilogue waits
 // (bounded) for the flags of the following clusters that hold the rest of the
-// tile, adds their partials in cluster order and stores the tile.  Owners only
-// wait on contributors and contributors wait on nobody, so there is no cycle;
-// all clusters are resident at once (the grid is capped at the clusters the
-// GPU can hold).
+// tile and adds their partials in cluster order before storing, while the
+// cluster's MMAs go on with its next tile.  When the owner unit is its
+// cluster's last (no data-parallel tiles), its epilogue warps instead sum the
+// partials into the spare TMEM accumulator while the owner's own MMAs run.
+// Owners only wait on contributors and contributors wait on nobody, so there
+// is no cycle; all clusters are resident at once (the grid is capped at the
+// clusters the GPU can hold).
 #pragma once
 
 #include "gemm_common.cuh"
@@ -245,13 +248,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
+            const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+            // stream-K owner: the clusters after this one whose units start inside
+            // this tile hold the rest of its K range
+            int q_end = cluster + 1;
+            bool prefetched = false;
+            if (k0 == 0 && k1 < KB) {
+                const long long tile_end = (long long)(t - p.dp_tiles + 1) * KB;
+                while (q_end < p.sk_pairs && sk_begin(p, q_end) < tile_end) ++q_end;
+                bool ok = true;
+                for (int qq = cluster + 1; ok && qq < q_end; ++qq) {
+                    const unsigned* f = p.flags + (qq * 2 + (int)rank) * 4 + q;
+                    int r = 1;
+                    if (lane == 0) r = wait_flag(f, p.epoch, abort_flag, 4 * p.wait_limit);
+                    ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+                    if (ok) (void)ptx::ld_acquire_gpu(f);  // orders this lane's reads after the flag
+                }
+                if (!ok) break;
+                // the owner unit is its cluster's last, so the other accumulator is
+                // free: sum the contributors' partials into it while the MMAs run
+                UnitIter peek = u;
+                int t2, a2, b2;
+                if (q_end > cluster + 1 && !unit_next(peek, p, t2, a2, b2)) {
+                    const uint32_t spare = lane_base + (uint32_t)((acc ^ 1) * kPairBN);
+#pragma unroll 1
+                    for (int c = 0; c < kPairBN / 32; ++c) {
+                        uint32_t x[32];
+                        for (int qq = cluster + 1; qq < q_end; ++qq) {
+                            const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
+                            uint32_t y[32];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                ptx::ld_global_cg_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), y[4 * j],
+                                                     y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                if (qq == cluster + 1)
+                                    x[i] = y[i];
+                                else
+                                    fadd_bits(x[i], y[i]);
+                            }
+                        }
+                        ptx::tmem_st_32x32b_x32(spare + (uint32_t)(c * 32), x);
+                    }
+                    ptx::tmem_st_wait();
+                    prefetched = true;
+                }
+            }
             if (KB > 0) {
                 if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane))
                     break;
                 ptx::tc_fence_after();
             }
             const int row0 = mb * kPairBM + (int)rank * kBM + q * 32;
-            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPairBN);
+            const uint32_t trow = lane_base + (uint32_t)(acc * kPairBN);
 
             if (k0 > 0) {
                 // stream-K contributor: park this CTA's partial (its 128 rows) in the
@@ -276,22 +326,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) ptx::st_release_gpu(p.flags + (cluster * 2 + (int)rank) * 4 + q, p.epoch);
                 continue;
             }
-            // stream-K owner: the clusters after this one whose units start inside
-            // this tile hold the rest of its K range
-            int q_end = cluster + 1;
-            if (k1 < KB) {
-                const long long tile_end = (long long)(t - p.dp_tiles + 1) * KB;
-                while (q_end < p.sk_pairs && sk_begin(p, q_end) < tile_end) ++q_end;
-                bool ok = true;
-                for (int qq = cluster + 1; ok && qq < q_end; ++qq) {
-                    const unsigned* f = p.flags + (qq * 2 + (int)rank) * 4 + q;
-                    int r = 1;
-                    if (lane == 0) r = wait_flag(f, p.epoch, abort_flag, 4 * p.wait_limit);
-                    ok = __shfl_sync(0xffffffffu, r, 0) != 0;
-                    if (ok) (void)ptx::ld_acquire_gpu(f);  // orders this lane's reads after the flag
-                }
-                if (!ok) break;
-            }
 #pragma unroll 1
             for (int c = 0; c < kPairBN / kCols; ++c) {
                 uint32_t v[kCols];
@@ -310,8 +344,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
                 }
-                // stream-K owner: add the contributors' partials, in cluster order
-                for (int qq = cluster + 1; qq < q_end; ++qq) {
+                // stream-K owner: add the contributors' partials (summed in cluster
+                // order), from the spare accumulator or straight from the workspace
+                if (prefetched) {
+                    uint32_t x[kCols];
+                    const uint32_t sp = lane_base + (uint32_t)((acc ^ 1) * kPairBN + c * kCols);
+                    ptx::tmem_ld_32x32b_x32(sp, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+                    if constexpr (OUT == 0) ptx::tmem_ld_32x32b_x32(sp + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
+                }
+                for (int qq = cluster + 1; !prefetched && qq < q_end; ++qq) {
                     const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
                     uint32_t x[kCols];
 #pragma unroll

@@ -2,15 +2,15 @@
 replayed on the CPU for the plans the planner makes.
 
 Mirrors the kernel's unit walk (data-parallel tiles c, c + clusters, ... below
-dp_tiles, then cluster c's even share [S c / P, S (c+1) / P) of the
+dp_tiles, after cluster c's even share [S c / P, S (c+1) / P) of the
 S = sk_tiles * k_steps stream-K iterations) and its owner rule (the unit that
 starts a tile but does not finish it waits for the following clusters whose
 shares start inside that tile).  Checked: every (tile, K step) is computed
 exactly once; each partly computed tile has one owner, whose contributor set
 is exactly the other units of that tile; a cluster contributes at most once
-(its first stream-K unit, which fixes its workspace slot) and owns at most
-once (its last unit), so owners wait only on contributors, which work at the
-start of the stream-K phase, and nothing waits on an owner.
+(its first unit of all, which fixes its workspace slot) and owns at most once
+(its last stream-K unit), so owners wait only on contributors, which work at
+the start of the launch, and nothing waits on an owner.
 """
 import pytest
 
@@ -19,20 +19,21 @@ import tensor_core_tiled_02_gb300 as tc
 
 def units_of(plan, c, clusters):
     KB = plan["k_steps"]
-    out = []
+    dp = []
     t = c
     while t < plan["dp_tiles"]:
-        out.append((t, 0, KB))
+        dp.append((t, 0, KB))
         t += clusters
+    sk = []
     if plan["sk_tiles"] and c < plan["sk_pairs"]:
         S = plan["sk_tiles"] * KB
         it, end = S * c // plan["sk_pairs"], S * (c + 1) // plan["sk_pairs"]
         while it < end:
             local, k0 = divmod(it, KB)
             k1 = min(KB, k0 + (end - it))
-            out.append((plan["dp_tiles"] + local, k0, k1))
+            sk.append((plan["dp_tiles"] + local, k0, k1))
             it += k1 - k0
-    return out
+    return sk + dp
 
 
 def check_plan(plan):
@@ -40,10 +41,8 @@ def check_plan(plan):
     KB = plan["k_steps"]
     cover = {}
     per_tile = {}
-    dp_units = {}
     for c in range(clusters):
         us = units_of(plan, c, clusters)
-        dp_units[c] = sum(1 for t, _, _ in us if t < plan["dp_tiles"])
         for i, (t, k0, k1) in enumerate(us):
             assert 0 <= t < plan["num_tiles"] and 0 <= k0 < k1 <= KB
             for k in range(k0, k1):
@@ -60,7 +59,8 @@ def check_plan(plan):
         owners = [u for u in units if u[3] == 0]
         assert len(owners) == 1
         oc, oi, on, _, ok1 = owners[0]
-        assert oi == on - 1, "an owner unit must be its cluster's last"
+        n_sk = sum(1 for tt, _, _ in units_of(plan, oc, clusters) if tt >= plan["dp_tiles"])
+        assert oi == n_sk - 1, "an owner unit must be its cluster's last stream-K unit"
         # the kernel's rule for the contributors of this tile
         tile_end = (t - plan["dp_tiles"] + 1) * KB
         q_end = oc + 1
@@ -70,7 +70,7 @@ def check_plan(plan):
         assert contributors == list(range(oc + 1, q_end))
         for c, i, n, k0, k1 in units:
             if k0 > 0:
-                assert i == dp_units[c], "a contributor unit must be its cluster's first stream-K unit"
+                assert i == 0, "a contributor unit must be its cluster's first unit"
                 assert c < plan["sk_pairs"]
 
 
