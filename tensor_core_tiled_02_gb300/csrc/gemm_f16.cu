@@ -49,8 +49,8 @@ int check_args(const void* A, const void* B, const void* C, int M, int N, int K,
     if (out_dtype != GEMM_OUT_F16 && out_dtype != GEMM_OUT_F32) return GEMM_ERR_DTYPE;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_DIM;
     if (N % 8 != 0 || K % 8 != 0) return GEMM_ERR_ALIGN;
-    // tile ids and tile coordinates must fit an int
-    if ((long long)ceil_div(M, kBM) * ceil_div(N, 128) > INT_MAX) return GEMM_ERR_DIM;
+    // tile ids and tile coordinates must fit an int, for the narrowest tile (64 columns)
+    if ((long long)ceil_div(M, kBM) * ceil_div(N, 64) > INT_MAX) return GEMM_ERR_DIM;
     if (M == 0 || N == 0) return 1;
     if (!check_ptrs) return GEMM_OK;
     if (!C || (K > 0 && (!A || !B))) return GEMM_ERR_NULL;
@@ -120,6 +120,13 @@ int max_slots_for_pair(int out_dtype, int step_k) {
     return s;
 }
 
+// Workspace of a stream-K plan shared by `ctas` CTAs: a flag per epilogue
+// warp of every CTA (rounded up to 256 bytes), then one fp32 partial of up to
+// 128 x 256 per CTA.
+size_t flag_bytes_for(int ctas) { return ((size_t)ctas * 4 * sizeof(unsigned) + 255) / 256 * 256; }
+
+size_t workspace_for(int ctas) { return flag_bytes_for(ctas) + (size_t)ctas * kPartialFloats * sizeof(float); }
+
 // The planner.
 // Tile: 128 x 256 or 128 x 128, whichever needs less time counted in waves of
 // tiles over the SMs, a 128 x 128 tile costing 0.85 of a 128 x 256 one (half
@@ -133,13 +140,6 @@ int max_slots_for_pair(int out_dtype, int step_k) {
 // emit_pipeline, stages must exceed release, and stages is clamped to the
 // steps one CTA runs (never below release + 1).  Default: the deepest ring
 // that fits shared memory.
-// Workspace of a stream-K plan shared by `ctas` CTAs: a flag per epilogue
-// warp of every CTA (rounded up to 256 bytes), then one fp32 partial of up to
-// 128 x 256 per CTA.
-size_t flag_bytes_for(int ctas) { return ((size_t)ctas * 4 * sizeof(unsigned) + 255) / 256 * 256; }
-
-size_t workspace_for(int ctas) { return flag_bytes_for(ctas) + (size_t)ctas * kPartialFloats * sizeof(float); }
-
 int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bool with_workspace,
               const gemm_config& cfg, gemm_plan* p) {
     std::memset(p, 0, sizeof(*p));

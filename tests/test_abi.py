@@ -70,6 +70,11 @@ def test_argument_errors_before_any_cuda_call(lib):
     assert _call(lib, M=-1) == DIM
     assert _call(lib, N=-8) == DIM
     assert _call(lib, K=-8) == DIM
+    # tile ids must fit an int for the narrowest tile, 128 x 64: 2^16 x 2^15 of them do not
+    assert _call(lib, M=1 << 23, N=1 << 21) == DIM
+    plan = tc.GemmPlan()
+    assert lib.gemm_f16_plan(1 << 23, 1 << 21, 64, 0, 152, ctypes.byref(plan)) == DIM
+    assert lib.gemm_f16_plan(1 << 23, 1 << 20, 64, 0, 152, ctypes.byref(plan)) == 0
     assert _call(lib, C=0) == NULL
     assert _call(lib, A=0) == NULL
     assert _call(lib, B=0) == NULL
