@@ -27,14 +27,35 @@ constexpr long long kDefaultWaitLimit = 2000000000LL;  // ~1 s at 2 GHz
 std::mutex g_mu;
 gemm_config g_cfg = {};
 
+// Per-device facts, filled on first use.  Fast paths read the atomics; the
+// first fill of each takes g_dev_mu, so concurrent first calls from several
+// host threads are safe.
 struct DeviceInfo {
-    bool ready = false;
+    std::atomic<bool> ready{false};
     int sms = 0;
     int cc = 0;
-    int max_pairs = 0;  // CTA-pair clusters the GPU holds at once (0: not yet asked)
-    bool attr_set[5][2] = {};  // [tile_n 64 / 128 / 256, CTA pair step K 64 / 128][out_dtype]
+    std::atomic<int> max_pairs{0};  // CTA-pair clusters the GPU holds at once (0: not yet asked)
+    // [tile_n 64 / 128 / 256, CTA pair step K 64 / 128, blocked add][out_dtype]: the
+    // kernel's shared-memory limit has been raised on this device
+    std::atomic<bool> attr_set[6][2];
 };
-DeviceInfo g_dev[kMaxDevices];
+DeviceInfo g_dev[kMaxDevices];  // static storage: every atomic starts zero
+std::mutex g_dev_mu;
+
+// Raise a kernel's dynamic shared-memory limit once per device.
+template <typename Kern>
+int ensure_smem_limit(Kern kern, int bytes, std::atomic<bool>& done) {
+    if (done.load(std::memory_order_acquire)) return GEMM_OK;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!done.load(std::memory_order_relaxed)) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+        done.store(true, std::memory_order_release);
+    }
+    return GEMM_OK;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<unsigned> g_epoch{0};  // stream-K flag value of the latest launch
@@ -249,9 +270,9 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bo
     // of all tiles are dealt out in equal contiguous shares to up to one CTA
     // per SM (at least 16 K steps each), partial tiles meeting through the
     // workspace.  Not a default: on one row of tiles (M = 128, N = K = 8192)
-    // it measured 34.5 us against 29.7 us for split-K clusters, because
-    // 128 SMs already saturate HBM there and a partial parked in global memory
-    // costs more than one pushed through distributed shared memory.
+    // it measured 34.5 us where split-K clusters take 28-30 us, because 128
+    // SMs already saturate HBM there and a partial parked in global memory
+    // costs more than one passed through distributed shared memory.
     if (cfg.split == 0 && cfg.grid == 0 && cfg.stream_k == 2 && p->k_steps > 0) {
         const long long iters = (long long)p->num_tiles * p->k_steps;
         long long ctas = iters / 16;
@@ -298,7 +319,9 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bo
     if (p->sk_tiles > 0) steps_per_cta = ((long long)p->sk_tiles * p->k_steps + p->sk_pairs - 1) / p->sk_pairs;
     if (steps_per_cta < s) s = (int)(steps_per_cta > d ? steps_per_cta : d + 1);
     if (split > 1) {
-        // the other ranks park an fp32 partial tile in their ring buffers
+        // partials of other ranks' chunks are parked in (more than two ranks)
+        // or pushed into (two ranks, 128 x 256 tiles) the ring: it must hold
+        // one fp32 tile
         const int stage_bytes = kBM * kBK * 2 + kBK * tn * 2;
         const int need = (kBM * tn * 4 + stage_bytes - 1) / stage_bytes;
         if (s + d < need) s = need - d;
@@ -344,17 +367,20 @@ int device_info(DeviceInfo** out) {
         return GEMM_ERR_CUDA;
     }
     DeviceInfo& d = g_dev[dev];
-    if (!d.ready) {
-        int sms = 0, major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_CUDA;
+    if (!d.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lk(g_dev_mu);
+        if (!d.ready.load(std::memory_order_relaxed)) {
+            int sms = 0, major = 0, minor = 0;
+            if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+                cudaGetLastError();
+                return GEMM_ERR_CUDA;
+            }
+            d.sms = sms;
+            d.cc = major * 10 + minor;
+            d.ready.store(true, std::memory_order_release);
         }
-        d.sms = sms;
-        d.cc = major * 10 + minor;
-        d.ready = true;
     }
     *out = &d;
     return GEMM_OK;
@@ -364,14 +390,8 @@ template <int OUT, int SK>
 int launch_pair(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
     auto kern = gemm_f16_pair_kernel<OUT, SK>;
-    bool& attr_done = dev.attr_set[SK == 128 ? 4 : 3][OUT];
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-        attr_done = true;
-    }
+    const int rc = ensure_smem_limit(kern, kSmemLimit, dev.attr_set[SK == 128 ? 4 : 3][OUT]);
+    if (rc != GEMM_OK) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(plan.grid, 1, 1);
     lc.blockDim = dim3(kThreads, 1, 1);
@@ -398,14 +418,8 @@ template <int BN, int OUT>
 int launch(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
            const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
     auto kern = gemm_f16_kernel<BN, OUT>;
-    bool& attr_done = dev.attr_set[BN == 64 ? 0 : BN == 128 ? 1 : 2][OUT];
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-        attr_done = true;
-    }
+    const int rc = ensure_smem_limit(kern, kSmemLimit, dev.attr_set[BN == 64 ? 0 : BN == 128 ? 1 : 2][OUT]);
+    if (rc != GEMM_OK) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(plan.grid, 1, 1);
     lc.blockDim = dim3(kThreads, 1, 1);
@@ -439,7 +453,10 @@ int launch(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, 
 // CTA-pair clusters the GPU can hold at once (stream-K owners wait on other
 // clusters, so every cluster of a launch must be resident together).
 int max_pairs_of(DeviceInfo& dev) {
-    if (dev.max_pairs == 0) {
+    const int known = dev.max_pairs.load(std::memory_order_acquire);
+    if (known > 0) return known;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev.max_pairs.load(std::memory_order_relaxed) == 0) {
         cudaLaunchConfig_t lc = {};
         lc.gridDim = dim3(dev.sms, 1, 1);
         lc.blockDim = dim3(kThreads, 1, 1);
@@ -458,9 +475,9 @@ int max_pairs_of(DeviceInfo& dev) {
             cudaGetLastError();
             n = dev.sms / 2;
         }
-        dev.max_pairs = n < dev.sms / 2 ? n : dev.sms / 2;
+        dev.max_pairs.store(n < dev.sms / 2 ? n : dev.sms / 2, std::memory_order_release);
     }
-    return dev.max_pairs;
+    return dev.max_pairs.load(std::memory_order_relaxed);
 }
 
 gemm_config current_config() {
@@ -702,17 +719,9 @@ int add_matrices_f32(const float* X, const float* Y, float* Z, int M, int N, gem
     ap.slots = 3;  // at least 2: a slot is freed only after the next tile's store
     ap.wait_limit = cfg.wait_limit > 0 ? cfg.wait_limit : kDefaultWaitLimit;
     const int tiles = ap.tiles_m * ap.tiles_n;
-    static bool attr_done[kMaxDevices] = {};
-    int devno = 0;
-    cudaGetDevice(&devno);
     const int smem = AddLayout::smem_bytes(ap.slots);
-    if (!attr_done[devno]) {
-        if (cudaFuncSetAttribute(add_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
-            cudaGetLastError();
-            return GEMM_ERR_LAUNCH;
-        }
-        attr_done[devno] = true;
-    }
+    rc = ensure_smem_limit(add_f32_kernel, smem, dev->attr_set[5][0]);
+    if (rc != GEMM_OK) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(tiles < dev->sms ? tiles : dev->sms, 1, 1);
     lc.blockDim = dim3(kAddThreads, 1, 1);
