@@ -22,6 +22,8 @@
  *   - A, B and C are DEVICE pointers owned by the caller.  The library never
  *     allocates, frees or synchronises them; it keeps only a small per-device
  *     cache (SM count, kernel attributes) and one process-wide tuning config.
+ *   - Every entry point may be called from several host threads at once; the
+ *     cache is filled under a lock on first use.
  *   - Return value: 0 on success, a negative gemm_status code otherwise.
  *     Argument checks run on the host before any CUDA call; no exceptions are
  *     thrown and nothing is printed.
@@ -211,7 +213,8 @@ int gemm_f16_plan(int M, int N, int K, int out_dtype, int num_sms, gemm_plan *ou
 int gemm_f16_plan_ws(int M, int N, int K, int out_dtype, int num_sms, gemm_plan *out);
 
 /* Replace the process-wide tuning config (copied); NULL restores defaults.
- * Not synchronised with concurrent gemm_f16 calls on other host threads.
+ * A call running at the same time on another host thread plans with either
+ * the old or the new config, never a mix.
  * Errors: GEMM_ERR_CONFIG for an out-of-range field (the old config stays). */
 int gemm_f16_set_config(const gemm_config *cfg);
 
