@@ -171,10 +171,12 @@ int gemm_f16_ws(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N,
 
 /*
  * As gemm_f16_ws, for callers that cannot allocate device memory when they
- * call: code running while a CUDA graph is captured (cudaMalloc is not
- * allowed there), allocators and runtimes that must not re-enter the CUDA
- * allocator, plugins handed only their input and output buffers.  The pages
- * have no counterpart; this is an interface convenience of this library.
+ * call: a memory allocator or runtime that must not re-enter the CUDA
+ * allocator from inside its own calls; a plugin or operator that its host
+ * framework hands only input and output buffers, with no allocation hook; code
+ * on a latency-critical path, where cudaMalloc may synchronise the device.
+ * The pages have no counterpart; this is an interface convenience of this
+ * library.
  *
  * The stream-K scratch lives in one fixed array of 20 MiB in device memory,
  * which every GPU that loads this library holds until the process exits.

@@ -743,10 +743,10 @@ int add_matrices_f32(const float* X, const float* Y, float* Z, int M, int N, gem
 
 // ---- stream-K without any allocation ---------------------------------------------
 //
-// For callers that cannot allocate device memory at the point of the call: code
-// running while a CUDA graph is being captured, where cudaMalloc is not allowed;
+// For callers that cannot allocate device memory at the point of the call:
 // allocators or runtimes that must not re-enter the CUDA allocator; plugins
-// that are handed only their input and output buffers.  gemm_f16_noalloc runs
+// that are handed only their input and output buffers; latency-critical code
+// where cudaMalloc may synchronise the device.  gemm_f16_noalloc runs
 // the same plan as gemm_f16_ws, with the stream-K scratch (flags and fp32
 // partial tiles) in one fixed array in device memory instead of a workspace
 // the caller passes in.

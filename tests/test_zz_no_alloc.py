@@ -1,7 +1,8 @@
 """gemm_f16_noalloc: the entry point for callers that cannot allocate device
-memory when they call (during CUDA graph capture, inside an allocator, in a
-plugin handed only its buffers).  Its stream-K scratch is a fixed array in
-device memory, shared by all calls.
+memory when they call (an allocator that must not re-enter the CUDA
+allocator, a plugin handed only its buffers, latency-critical code where
+cudaMalloc may synchronise the device).  Its stream-K scratch is a fixed
+array in device memory, shared by all calls.
 
 Called through the C ABI, it must give what gemm_f16_ws gives with a
 caller-owned workspace, within the parity tolerance, on two calls in a row
