@@ -70,8 +70,10 @@ __global__ void __launch_bounds__(kAddThreads, 1)
         ptx::prefetch_tmap(&tmZ);
     }
     __syncthreads();
-    ptx::grid_dependency_wait();
-    ptx::grid_launch_dependents();
+    // each role waits for the previous kernel in the stream just before its
+    // first global-memory access: the producer before its first load (its
+    // set-up runs earlier, overlapping that kernel), the adding warps before
+    // their first store
 
     const int num_tiles = p.tiles_m * p.tiles_n;
     if (warp == 0) {
@@ -79,12 +81,18 @@ __global__ void __launch_bounds__(kAddThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
+            bool dep_done = false;
             for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
                 if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) break;
                 const int x = (t % p.tiles_n) * kAddBN;
                 const int y = (t / p.tiles_n) * kAddBM;
                 const uint32_t fb = full_bar(stage);
                 ptx::mbar_arrive_expect_tx(fb, 2 * kAddTileBytes);
+                if (!dep_done) {
+                    ptx::grid_dependency_wait();
+                    ptx::grid_launch_dependents();
+                    dep_done = true;
+                }
                 ptx::tma_load_2d(sX + stage * kAddTileBytes, &tmX, fb, x, y);
                 ptx::tma_load_2d(sY + stage * kAddTileBytes, &tmY, fb, x, y);
                 issued_mask |= 1u << stage;
@@ -99,6 +107,8 @@ __global__ void __launch_bounds__(kAddThreads, 1)
                 if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_phase >> s) & 1u, p.wait_limit);
         }
     } else {
+        ptx::grid_dependency_wait();
+        ptx::grid_launch_dependents();
         const int w = warp - 1;               // this warp's rows: 8w .. 8w+7 of the tile
         constexpr int kRows = kAddBM / kAddWarps;
         constexpr int kVec = kRows * kAddBN / 4 / 32;  // 16-byte groups per lane

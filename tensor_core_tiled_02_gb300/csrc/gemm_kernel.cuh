@@ -55,8 +55,14 @@
 // the grid never exceeds the CTAs the GPU holds at once.
 //
 // Programmatic dependent launch: the prologue (barriers, TMEM, tensor-map
-// prefetch) runs before `griddepcontrol.wait`, so it overlaps the tail of the
-// previous kernel in the stream; no global memory is touched before the wait.
+// prefetch) and the producer's set-up of its first load (tile walk, first ring
+// slot, expect-tx) run before `griddepcontrol.wait`, so they overlap the tail
+// of the previous kernel in the stream.  Each role waits just before its first
+// global-memory access: the producer before its first TMA load, the epilogue
+// on entering its role; the MMA warp touches only shared and tensor memory
+// and never waits.  The set-up is worth moving: the first pass through each
+// code path misses the instruction cache, about 500 cycles a time, and on
+// the critical path after the wait those misses cost ~0.85 us per launch.
 //
 // Roles (192 threads, one CTA per SM):
 //   warp 0       TMA producer (one lane)
@@ -149,9 +155,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (split > 1) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // the previous kernel's writes (and reads) of A, B and C are done from here on
-    ptx::grid_dependency_wait();
-    ptx::grid_launch_dependents();
 
     // this CTA's cluster (itself without split-K) and the clusters of the grid
     const int cl = blockIdx.x / split;
@@ -170,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;  // per slot: ever issued, parity of last issue
             bool ok = true;
+            bool dep_done = false;
             UnitIter u;
             unit_iter_init(u, p, cl, clusters);
             int t, k0, k1;
@@ -184,6 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t fb = full_bar(stage);
                     ptx::mbar_arrive_expect_tx(fb, L::kStageBytes);
+                    if (!dep_done) {
+                        // the previous kernel's writes of A and B are done from here on
+                        ptx::grid_dependency_wait();
+                        ptx::grid_launch_dependents();
+                        dep_done = true;
+                    }
                     ptx::tma_load_2d(sA + stage * L::kABytes, &tmA, fb, kb * kBK, mb * kBM);
 #pragma unroll
                     for (int j = 0; j < BN / 64; ++j)
@@ -266,6 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (split > 1) ptx::cluster_arrive();
     } else {
         // ---------------- epilogue: TMEM -> registers -> SMEM -> TMA store ----------------
+        // the previous kernel's reads and writes of C (and of the workspace) are
+        // done from here on
+        ptx::grid_dependency_wait();
+        ptx::grid_launch_dependents();
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t staging = sC + (uint32_t)(q * 2 * L::kStagingBytes);
         const int row_in_tile = q * 32 + lane;

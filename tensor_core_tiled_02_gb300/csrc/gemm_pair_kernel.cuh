@@ -19,7 +19,9 @@
 //   - each CTA's epilogue drains its own 128 x 256 block exactly as the
 //     single-CTA kernel does.
 // Persistent: cluster c walks pair tiles c, c + clusters, ... in the grouped
-// raster.  Programmatic dependent launch as in the single-CTA kernel.
+// raster.  Programmatic dependent launch as in the single-CTA kernel: the
+// producer waits for the previous kernel just before its first TMA load, the
+// epilogue on entering its role, the MMA warp never.
 //
 // Stream-K (sk_tiles > 0): the K iterations of the tiles beyond the full
 // waves are split evenly over the first sk_pairs clusters, which run their
@@ -122,8 +124,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    ptx::grid_dependency_wait();
-    ptx::grid_launch_dependents();
 
     const int cluster = blockIdx.x >> 1;   // this pair
     const int clusters = gridDim.x >> 1;
@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
+            bool dep_done = false;
             UnitIter u;
             unit_iter_init(u, p, cluster, clusters);
             int t, k0, k1;
@@ -152,6 +153,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb_local = full_bar(stage);
                     if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * L::kStageBytes);
                     const uint32_t fb = ptx::mapa(fb_local, 0);
+                    if (!dep_done) {
+                        // the previous kernel's writes of A and B are done from here on
+                        ptx::grid_dependency_wait();
+                        ptx::grid_launch_dependents();
+                        dep_done = true;
+                    }
 #pragma unroll
                     for (int h = 0; h < SK / 64; ++h)
                         ptx::tma_load_2d_pair(sA + stage * L::kABytes + h * L::kAtomBytes, &tmA, fb, kb * SK + h * 64,
@@ -234,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue (both CTAs): own 128 rows x 256 columns ----------------
+        // the previous kernel's reads and writes of C and of the workspace are
+        // done from here on
+        ptx::grid_dependency_wait();
+        ptx::grid_launch_dependents();
         const int q = warp & 3;
         const uint32_t staging = sC + (uint32_t)(q * 2 * L::kStagingBytes);
         const int row_in_tile = q * 32 + lane;
