@@ -69,7 +69,8 @@ typedef enum {
 
 /* What the planner chose for one problem (gemm_f16_plan). */
 typedef struct {
-    int cta_group;              /* 1: one CTA per tile; 2: a CTA pair (two SMs) per tile */
+    int cta_group;              /* 1: one CTA per tile; 2: a CTA pair (two SMs) per tile,
+                                   256 x 256 or 128 x 128 */
     int tile_m, tile_n, tile_k; /* output tile and K step (elements) */
     int tiles_m, tiles_n;       /* ceil(M/tile_m), ceil(N/tile_n) */
     int num_tiles;              /* tiles_m * tiles_n: one owner CTA each */
@@ -99,10 +100,11 @@ typedef struct {
     int raster_group;      /* 0 or >= 1 */
     long long wait_limit;  /* 0 = about one second; else clock cycles one device wait may take */
     int split;             /* 0 = planner default; 1 = no split-K; 2..8 = CTAs per tile along K */
-    int cta_group;         /* 0 = planner default; 1 = one CTA per tile; 2 = CTA pairs
-                              (256 x 256 tiles; needs tile_n 0 or 256 and no split) */
+    int cta_group;         /* 0 = planner default; 1 = one CTA per tile; 2 = CTA pairs, no
+                              split: 256 x 256 tiles (tile_n 0 or 256; 128 rows per SM)
+                              or 128 x 128 tiles (tile_n 128; 64 rows per SM) */
     int tile_k;            /* 0 = planner default; K depth of one pipeline step: 64, or 128
-                              (CTA pairs only) */
+                              (CTA pairs only; 128 x 128 pair tiles take 128 only) */
     int stream_k;          /* 0 = planner default (gemm_f16_ws shares the last, partly
                               filled wave of CTA-pair tiles); 1 = never; 2 = share the K
                               iterations of every tile, also on single CTAs (needs a

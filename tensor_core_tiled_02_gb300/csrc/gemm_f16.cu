@@ -37,7 +37,7 @@ struct DeviceInfo {
     std::atomic<int> max_pairs{0};  // CTA-pair clusters the GPU holds at once (0: not yet asked)
     // [tile_n 64 / 128 / 256, CTA pair step K 64 / 128, blocked add][out_dtype]: the
     // kernel's shared-memory limit has been raised on this device
-    std::atomic<bool> attr_set[6][2];
+    std::atomic<bool> attr_set[7][2];
 };
 DeviceInfo g_dev[kMaxDevices];  // static storage: every atomic starts zero
 std::mutex g_dev_mu;
@@ -98,7 +98,9 @@ int check_config(const gemm_config& c) {
     if (c.inject_stall != 0 && c.inject_stall != 1) return GEMM_ERR_CONFIG;
     if (c.split < 0 || c.split > kMaxSplit) return GEMM_ERR_CONFIG;
     if (c.cta_group < 0 || c.cta_group > 2) return GEMM_ERR_CONFIG;
-    if (c.cta_group == 2 && ((c.tile_n != 0 && c.tile_n != 256) || c.split > 1)) return GEMM_ERR_CONFIG;
+    // CTA pairs: tile_n 0 or 256 for 256 x 256 tiles, 128 for 128 x 128 tiles
+    if (c.cta_group == 2 && ((c.tile_n != 0 && c.tile_n != 128 && c.tile_n != 256) || c.split > 1))
+        return GEMM_ERR_CONFIG;
     if (c.tile_k != 0 && c.tile_k != 64 && c.tile_k != 128) return GEMM_ERR_CONFIG;
     if (c.stream_k < 0 || c.stream_k > 2) return GEMM_ERR_CONFIG;
     return GEMM_OK;
@@ -122,7 +124,11 @@ int smem_request(int smem_bytes, int tmem_cols) {
     return smem_bytes > floor_bytes ? smem_bytes : floor_bytes;
 }
 
-int smem_for_pair(int out_dtype, int step_k, int slots) {
+// pair_m: the pair's tile, 256 (256 x 256) or 128 (128 x 128, 128-deep steps only)
+int smem_for_pair(int out_dtype, int step_k, int pair_m, int slots) {
+    if (pair_m == 128)
+        return out_dtype == GEMM_OUT_F16 ? PairLayout<0, 128, 128, 128>::smem_bytes(slots)
+                                         : PairLayout<1, 128, 128, 128>::smem_bytes(slots);
     if (step_k == 128)
         return out_dtype == GEMM_OUT_F16 ? PairLayout<0, 128>::smem_bytes(slots)
                                          : PairLayout<1, 128>::smem_bytes(slots);
@@ -135,9 +141,9 @@ int max_slots_for(int tile_n, int out_dtype) {
     return s;
 }
 
-int max_slots_for_pair(int out_dtype, int step_k) {
+int max_slots_for_pair(int out_dtype, int step_k, int pair_m) {
     int s = kMaxStages;
-    while (s > 1 && smem_for_pair(out_dtype, step_k, s) > kSmemLimit) --s;
+    while (s > 1 && smem_for_pair(out_dtype, step_k, pair_m, s) > kSmemLimit) --s;
     return s;
 }
 
@@ -183,27 +189,50 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bo
     // wins and no split is wanted, if its waves cost no more than 1/0.9 of the
     // single-CTA waves (it moves a third less operand data per SM and step).
     int cg = cfg.cta_group;
+    int pm = cg == 2 && cfg.tile_n == 128 ? 128 : 256;  // CTA pairs: 256 x 256 or 128 x 128 tiles
     if (cg == 0) {
         cg = 1;
+        const long long tiles128 = (long long)tiles_m * ceil_div(N, 128);
         if (tn == 256 && cfg.tile_n == 0 && cfg.split <= 1 && p->k_steps > 0 && num_sms >= 2) {
             const long long pair_tiles = (long long)ceil_div(M, 2 * kBM) * ceil_div(N, 256);
             const long long w_pair = (pair_tiles + num_sms / 2 - 1) / (num_sms / 2);
             const long long w_one = ((long long)p->num_tiles + num_sms - 1) / num_sms;
-            const long long tiles128 = (long long)tiles_m * ceil_div(N, 128);
             if (w_pair * 9 <= w_one * 10 && 2 * tiles128 > num_sms) cg = 2;
+        }
+        // Small problems: 128 x 128 tiles on CTA pairs (M = 128 over two SMs,
+        // 64 rows each) when they all fit one wave of pairs and one-CTA tiles
+        // would not split K: twice the CTAs of one-CTA tiles, each loading half
+        // the operands.  Not where split-K applies: streaming B from HBM (one
+        // row of tiles, N = K = 8192) the pair tiles took 33.7 us against
+        // 27.5 us for split-K over two CTAs (each pair steps in lock-step on
+        // both SMs' loads, and each CTA reads B rows 128 bytes at a time).
+        if (cg == 1 && cfg.tile_n == 0 && cfg.split == 0 && cfg.grid == 0 && cfg.stream_k != 2 &&
+            p->k_steps > 0 && num_sms >= 2 && tiles128 <= max_pairs) {
+            long long split1 = 1;
+            if (2 * tiles128 <= num_sms) {
+                split1 = num_sms / tiles128;
+                if (split1 > kMaxSplit) split1 = kMaxSplit;
+                if (split1 > p->k_steps / 16) split1 = p->k_steps / 16;
+            }
+            if (split1 <= 1) {
+                cg = 2;
+                pm = 128;
+            }
         }
     }
     if (cg == 2) {
         if (p->k_steps == 0 || num_sms < 2) return GEMM_ERR_CONFIG;
-        // 128-deep steps (eight MMAs per barrier wait and commit) unless K is short
-        const int sk = cfg.tile_k > 0 ? cfg.tile_k : (K >= 256 ? 128 : kBK);
+        // 128-deep steps (eight MMAs per barrier wait and commit) unless K is
+        // short; 128 x 128 pair tiles always take 128-deep steps
+        if (pm == 128 && cfg.tile_k != 0 && cfg.tile_k != 128) return GEMM_ERR_CONFIG;
+        const int sk = pm == 128 ? 128 : cfg.tile_k > 0 ? cfg.tile_k : (K >= 256 ? 128 : kBK);
         p->cta_group = 2;
         p->tile_k = sk;
         p->k_steps = ceil_div(K, sk);
-        p->tile_m = 2 * kBM;
-        p->tile_n = 256;
-        p->tiles_m = ceil_div(M, 2 * kBM);
-        p->tiles_n = ceil_div(N, 256);
+        p->tile_m = pm;
+        p->tile_n = pm;
+        p->tiles_m = ceil_div(M, pm);
+        p->tiles_n = ceil_div(N, pm);
         p->num_tiles = p->tiles_m * p->tiles_n;
         p->split = 1;
         if (cfg.grid > 0 && cfg.grid / 2 < max_pairs) max_pairs = cfg.grid / 2 > 0 ? cfg.grid / 2 : 1;
@@ -247,7 +276,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bo
         }
         p->grid = 2 * pairs;
         const int d = cfg.release;
-        const int max_slots = max_slots_for_pair(out_dtype, sk);
+        const int max_slots = max_slots_for_pair(out_dtype, sk, pm);
         int s = cfg.stages > 0 ? cfg.stages : max_slots - d;
         if (s <= d || s + d > max_slots) return GEMM_ERR_CONFIG;
         long long steps_per_cta = (long long)p->k_steps * ceil_div(p->num_tiles, pairs);
@@ -257,8 +286,8 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bo
         p->release = d;
         p->slots = s + d;
         p->raster_group = cfg.raster_group > 0 ? cfg.raster_group : 8;
-        p->tmem_cols = 512;
-        p->smem_bytes = smem_request(smem_for_pair(out_dtype, sk, p->slots), p->tmem_cols);
+        p->tmem_cols = pm == 256 ? 512 : 128;
+        p->smem_bytes = smem_request(smem_for_pair(out_dtype, sk, pm, p->slots), p->tmem_cols);
         p->threads = kThreads;
         return GEMM_OK;
     }
@@ -386,11 +415,11 @@ int device_info(DeviceInfo** out) {
     return GEMM_OK;
 }
 
-template <int OUT, int SK>
+template <int OUT, int SK, int PM = kPairBM, int PN = kPairBN>
 int launch_pair(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
-    auto kern = gemm_f16_pair_kernel<OUT, SK>;
-    const int rc = ensure_smem_limit(kern, kSmemLimit, dev.attr_set[SK == 128 ? 4 : 3][OUT]);
+    auto kern = gemm_f16_pair_kernel<OUT, SK, PM, PN>;
+    const int rc = ensure_smem_limit(kern, kSmemLimit, dev.attr_set[PM == 128 ? 6 : SK == 128 ? 4 : 3][OUT]);
     if (rc != GEMM_OK) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(plan.grid, 1, 1);
@@ -507,7 +536,9 @@ int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, 
     std::memset(&ta, 0, sizeof(ta));
     std::memset(&tb, 0, sizeof(tb));
     if (K > 0) {
-        rc = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, kBK, kBM);
+        // each CTA loads its rows of the tile: 128, or 64 on a 128 x 128 pair tile
+        rc = encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, kBK,
+                       (uint32_t)(plan.tile_m / plan.cta_group));
         if (rc != GEMM_OK) return rc;
         rc = encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, (uint64_t)N, (uint64_t)K, 64, plan.tile_k);
         if (rc != GEMM_OK) return rc;
@@ -547,6 +578,9 @@ int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, 
     }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan.cta_group == 2 && plan.tile_m == 128)
+        return out_dtype == GEMM_OUT_F16 ? launch_pair<0, 128, 128, 128>(plan, ta, tb, tc, kp, s, *dev)
+                                         : launch_pair<1, 128, 128, 128>(plan, ta, tb, tc, kp, s, *dev);
     if (plan.cta_group == 2 && plan.tile_k == 128)
         return out_dtype == GEMM_OUT_F16 ? launch_pair<0, 128>(plan, ta, tb, tc, kp, s, *dev)
                                          : launch_pair<1, 128>(plan, ta, tb, tc, kp, s, *dev);

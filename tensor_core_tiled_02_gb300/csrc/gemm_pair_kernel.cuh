@@ -1,23 +1,31 @@
 // The fp16 GEMM on a CTA pair (cta_group::2): a cluster of two CTAs on two
-// SMs owns each 256 x 256 output tile.
+// SMs owns each PM x PN output tile, 256 x 256 for large problems and
+// 128 x 128 for small ones.
 //
 // Same method as gemm_kernel.cuh (parallel grid of tiles, K pipeline through
 // an mbarrier-guarded shared-memory ring, fp32 accumulator in TMEM, drain
 // through shared memory and TMA; "Quickstart: GPU", section "Pipelining: a
 // matmul kernel"), with the tile split over two SMs:
-//   - CTA r (r = rank in the cluster) loads A rows [256 mb + 128 r, +128) and
-//     B columns [256 nb + 128 r, +128) of each K step: 32 KiB per step each,
-//     where a 128 x 256 tile on one SM needs 48 KiB;
-//   - one thread of the even CTA issues tcgen05.mma.cta_group::2 with M = 256,
-//     N = 256: each SM's tensor core takes its 128 rows of A from its own
-//     shared memory and the two halves of B from both, and writes its 128
-//     rows of D into its own TMEM;
+//   - CTA r (r = rank in the cluster) loads A rows [PM mb + PM/2 r, +PM/2)
+//     and B columns [PN nb + PN/2 r, +PN/2) of each K step (256 x 256: 32 KiB
+//     per 64-deep step each, where a 128 x 256 tile on one SM needs 48 KiB);
+//   - one thread of the even CTA issues tcgen05.mma.cta_group::2 with M = PM,
+//     N = PN: each SM's tensor core takes its PM/2 rows of A from its own
+//     shared memory and the two halves of B from both, and writes its PM/2
+//     rows of D into its own TMEM.  With M = 256 a CTA's 128 rows sit in the
+//     128 TMEM lanes, all PN columns across.  With M = 128 its 64 rows are
+//     folded over the lanes: lanes 0-63 hold columns 0 .. PN/2-1 of rows
+//     0-63, lanes 64-127 columns PN/2 .. PN-1 of the same rows, in PN/2 TMEM
+//     columns; so all four lane quadrants stay busy, and no partial sums
+//     change hands as they do under split-K;
 //   - both CTAs' loads count on the even CTA's `full` barrier (the leader arms
 //     it for both); the MMA commits release the slot in both CTAs and signal
 //     both epilogues (multicast); both CTAs' epilogue warps hand the
 //     accumulator back on the even CTA's `tmem_empty` barrier;
-//   - each CTA's epilogue drains its own 128 x 256 block exactly as the
-//     single-CTA kernel does.
+//   - each CTA's epilogue drains its own PM/2 x PN block as the single-CTA
+//     kernel does: epilogue warp q reads TMEM lanes 32q .. 32q+31, which hold
+//     rows 32q .. of the block (M = 256), or rows 32 (q % 2) .. and columns
+//     PN/2 (q / 2) .. (M = 128).
 // Persistent: cluster c walks pair tiles c, c + clusters, ... in the grouped
 // raster.  Programmatic dependent launch as in the single-CTA kernel: the
 // producer waits for the previous kernel just before its first TMA load, the
@@ -44,34 +52,39 @@
 
 namespace tcgemm {
 
-constexpr int kPairBM = 256;  // tile rows per pair (MMA M)
-constexpr int kPairBN = 256;  // tile columns per pair (MMA N)
+constexpr int kPairBM = 256;  // tile rows per pair (MMA M) of the large-problem variant
+constexpr int kPairBN = 256;  // tile columns per pair (MMA N) of the large-problem variant
 static_assert(kPartialFloats == kBM * kPairBN, "one CTA's partial of a pair tile");
 
 // SK: K depth of one pipeline step, 64 or 128.  A deeper step issues twice
 // the MMAs per barrier wait and per commit, with the same bytes in flight.
-template <int OUT, int SK = kBK>
+// PM x PN: the pair's tile, 256 x 256 or 128 x 128.
+template <int OUT, int SK = kBK, int PM = kPairBM, int PN = kPairBN>
 struct PairLayout {
     static_assert(SK == 64 || SK == 128, "step K");
-    static constexpr int kAtomBytes = kBM * 64 * 2;          // 128 rows x one 128-byte swizzle row
-    static constexpr int kABytes = kBM * SK * 2;             // this CTA's 128 rows: SK/64 atoms
+    static_assert((PM == 256 && PN == 256) || (PM == 128 && PN == 128), "pair tile");
+    static constexpr int kRows = PM / 2;                     // rows of A and D per CTA
+    static constexpr int kAtomBytes = kRows * 64 * 2;        // kRows rows x one 128-byte swizzle row
+    static constexpr int kABytes = kRows * SK * 2;           // this CTA's rows: SK/64 atoms
     static constexpr int kBBoxBytes = SK * 64 * 2;           // 64 columns x SK rows of B
-    static constexpr int kBBytes = 2 * kBBoxBytes;           // this CTA's 128 columns of B
+    static constexpr int kBBoxes = PN / 2 / 64;              // this CTA's PN/2 columns of B
+    static constexpr int kBBytes = kBBoxes * kBBoxBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kOutCols = OUT == 0 ? 64 : 32;
     static constexpr int kStagingBytes = 32 * 128;
-    static constexpr int kTmemCols = 2 * kPairBN;  // two 256-column accumulators: all 512
+    static constexpr int kAccCols = PM == 256 ? PN : PN / 2;  // TMEM columns of one accumulator
+    static constexpr int kTmemCols = 2 * kAccCols;            // two accumulators (256 x 256: all 512)
     // full[8], empty[8], tmem_full[2], tmem_empty[2], drain
     static constexpr int kNumBars = 2 * kMaxStages + 5;
     static constexpr int kFixedBytes = 4 * 2 * kStagingBytes + kNumBars * 8 + 16;
     static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
 };
 
-template <int OUT, int SK>
+template <int OUT, int SK, int PM = kPairBM, int PN = kPairBN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
-    using L = PairLayout<OUT, SK>;
+    using L = PairLayout<OUT, SK, PM, PN>;
     constexpr int kCols = L::kOutCols;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -143,8 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ok && unit_next(u, p, t, k0, k1)) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
-                const int m0 = mb * kPairBM + (int)rank * kBM;
-                const int n0 = nb * kPairBN + (int)rank * (kPairBN / 2);
+                const int m0 = mb * PM + (int)rank * L::kRows;
+                const int n0 = nb * PN + (int)rank * (PN / 2);
                 for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
                         ok = false;
@@ -163,8 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < SK / 64; ++h)
                         ptx::tma_load_2d_pair(sA + stage * L::kABytes + h * L::kAtomBytes, &tmA, fb, kb * SK + h * 64,
                                               m0);
-                    ptx::tma_load_2d_pair(sB + stage * L::kBBytes, &tmB, fb, n0, kb * SK);
-                    ptx::tma_load_2d_pair(sB + stage * L::kBBytes + L::kBBoxBytes, &tmB, fb, n0 + 64, kb * SK);
+#pragma unroll
+                    for (int j = 0; j < L::kBBoxes; ++j)
+                        ptx::tma_load_2d_pair(sB + stage * L::kBBytes + j * L::kBBoxBytes, &tmB, fb, n0 + j * 64,
+                                              kb * SK);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -182,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer (leader only) ----------------
         if (lane == 0 && rank == 0 && KB > 0) {
-            constexpr uint32_t idesc = make_idesc(kPairBM, kPairBN);
+            constexpr uint32_t idesc = make_idesc(PM, PN);
             int stage = 0;
             uint32_t phase = 0;
             long long it = 0;
@@ -200,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kPairBN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * L::kAccCols);
                 for (int kb = k0; kb < k1; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit, kSiteMmaFull)) {
                         ok = false;
@@ -217,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int k = 0; k < SK / kUmmaK; ++k) {
                         // A K-major: slice k is 32 bytes along the swizzled row of atom k/4.
                         // B MN-major: slice k is two 8-row groups (2 KiB) further down;
-                        // the two 64-wide column blocks are one box apart.
+                        // the 64-wide column blocks are one box apart.
                         const uint64_t ad = ad0 + (uint64_t)(((k / 4) * L::kAtomBytes + (k % 4) * (kUmmaK * 2)) >> 4);
                         const uint64_t bd = bd0 + (uint64_t)((k * (kUmmaK * 128)) >> 4);
                         ptx::mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb != k0) || (k != 0));
@@ -240,14 +255,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_drain(drain_bar, 0, p.wait_limit);
         }
     } else {
-        // ---------------- epilogue (both CTAs): own 128 rows x 256 columns ----------------
+        // ---------------- epilogue (both CTAs): own PM/2 rows x PN columns ----------------
         // the previous kernel's reads and writes of C and of the workspace are
         // done from here on
         ptx::grid_dependency_wait();
         ptx::grid_launch_dependents();
         const int q = warp & 3;
         const uint32_t staging = sC + (uint32_t)(q * 2 * L::kStagingBytes);
-        const int row_in_tile = q * 32 + lane;
+        const int row_in_tile = q * 32 + lane;  // TMEM lane: the workspace's row index
+        // this warp's block of the CTA's PM/2 x PN: rows wrow .., columns wcol ..
+        const int wrow = PM == 256 ? q * 32 : (q & 1) * 32;
+        const int wcol = PM == 256 ? 0 : (q >> 1) * (PN / 2);
         int tl = 0;
         int nstore = 0;
         UnitIter u;
@@ -281,9 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 UnitIter peek = u;
                 int t2, a2, b2;
                 if (q_end > cluster + 1 && !unit_next(peek, p, t2, a2, b2)) {
-                    const uint32_t spare = lane_base + (uint32_t)((acc ^ 1) * kPairBN);
+                    const uint32_t spare = lane_base + (uint32_t)((acc ^ 1) * L::kAccCols);
 #pragma unroll 1
-                    for (int c = 0; c < kPairBN / 32; ++c) {
+                    for (int c = 0; c < L::kAccCols / 32; ++c) {
                         uint32_t x[32];
                         for (int qq = cluster + 1; qq < q_end; ++qq) {
                             const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
@@ -311,16 +329,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 ptx::tc_fence_after();
             }
-            const int row0 = mb * kPairBM + (int)rank * kBM + q * 32;
-            const uint32_t trow = lane_base + (uint32_t)(acc * kPairBN);
+            const int row0 = mb * PM + (int)rank * L::kRows + wrow;
+            const int col0 = nb * PN + wcol;
+            const uint32_t trow = lane_base + (uint32_t)(acc * L::kAccCols);
 
             if (k0 > 0) {
-                // stream-K contributor: park this CTA's partial (its 128 rows) in the
-                // cluster's workspace slot as [column / 4][row] 16-byte groups
+                // stream-K contributor: park this CTA's partial in the cluster's
+                // workspace slot as [TMEM column / 4][TMEM lane] 16-byte groups
                 // (consecutive lanes, consecutive 16 bytes), then release the flag
                 float* slot = p.ws + (size_t)(cluster * 2 + (int)rank) * kPartialFloats;
 #pragma unroll 1
-                for (int c = 0; c < kPairBN / 32; ++c) {
+                for (int c = 0; c < L::kAccCols / 32; ++c) {
                     uint32_t v[32];
                     ptx::tmem_ld_32x32b_x32(trow + c * 32, v);
                     ptx::tmem_ld_wait();
@@ -338,14 +357,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
 #pragma unroll 1
-            for (int c = 0; c < kPairBN / kCols; ++c) {
+            for (int c = 0; c < L::kAccCols / kCols; ++c) {
                 uint32_t v[kCols];
                 if (KB > 0) {
                     ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                     if constexpr (OUT == 0)
                         ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                     ptx::tmem_ld_wait();
-                    if (c == kPairBN / kCols - 1) {
+                    if (c == L::kAccCols / kCols - 1) {
                         // this CTA's half of the accumulator is read: tell the leader
                         ptx::tc_fence_before();
                         __syncwarp();
@@ -359,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // order), from the spare accumulator or straight from the workspace
                 if (prefetched) {
                     uint32_t x[kCols];
-                    const uint32_t sp = lane_base + (uint32_t)((acc ^ 1) * kPairBN + c * kCols);
+                    const uint32_t sp = lane_base + (uint32_t)((acc ^ 1) * L::kAccCols + c * kCols);
                     ptx::tmem_ld_32x32b_x32(sp, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
                     if constexpr (OUT == 0) ptx::tmem_ld_32x32b_x32(sp + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
                     ptx::tmem_ld_wait();
@@ -376,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                 }
-                add_c_in<OUT>(v, p, row0 + lane, nb * kPairBN + c * kCols);
-                store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * kPairBN + c * kCols, row0);
+                add_c_in<OUT>(v, p, row0 + lane, col0 + c * kCols);
+                store_chunk<OUT>(v, &tmC, staging, nstore, lane, col0 + c * kCols, row0);
             }
         }
         if (lane == 0) ptx::bulk_wait_group_read<0>();

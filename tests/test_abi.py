@@ -97,16 +97,18 @@ def test_empty_problems_are_noops(lib):
 
 
 def test_plan_matches_the_tiling_arithmetic(lib):
-    """Sequential steps = K / tile_k for each workload; one CTA per output tile;
-    tiles = ceil(M/128) * ceil(N/tile_n)."""
+    """Sequential steps = K / tile_k for each workload; one CTA (or CTA pair)
+    per output tile; tiles = ceil(M/tile_m) * ceil(N/tile_n)."""
     # sequential steps of 64 (one CTA per tile) or 128 (CTA pairs) along K
-    want_k_steps = {"gemm_256": 4, "gemm_4096": 32, "gemm_8192": 64, "skinny": 128, "long_k": 256}
+    want_k_steps = {"gemm_256": 2, "gemm_4096": 32, "gemm_8192": 64, "skinny": 128, "long_k": 256}
     for name, w in WORKLOADS.items():
         if w.kind != "gemm":
             continue
         p = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, num_sms=152)
         assert p["k_steps"] == want_k_steps[name] == w.K // p["tile_k"]
-        assert p["tile_m"] == 128 * p["cta_group"] and p["tile_k"] == 64 * p["cta_group"]
+        assert p["tile_k"] == 64 * p["cta_group"]
+        assert (p["tile_m"], p["tile_n"]) in ({1: [(128, 64), (128, 128), (128, 256)],
+                                                2: [(256, 256), (128, 128)]}[p["cta_group"]])
         assert p["tiles_m"] == -(-w.M // p["tile_m"]) and p["tiles_n"] == -(-w.N // p["tile_n"])
         assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
         if p["cta_group"] == 2:  # one cluster of two CTAs per pair tile, persistent
@@ -118,9 +120,21 @@ def test_plan_matches_the_tiling_arithmetic(lib):
         assert 1 <= p["stages"] <= 8 and p["release"] < p["stages"]
         assert p["slots"] == p["stages"] + p["release"]
         assert p["smem_bytes"] <= 232448
-    # the 256^3 case is 2 x 2 tiles of 128 x 128 with 4 K steps
+    # the 256^3 case is 2 x 2 tiles of 128 x 128, each on a CTA pair (64 rows per
+    # SM) with 2 K steps of 128; on single CTAs, the pages' tiling: 4 K steps of 64
     p = tc.gemm_f16_plan(256, 256, 256, 0, num_sms=152)
-    assert (p["tiles_m"], p["tiles_n"], p["tile_n"], p["k_steps"], p["cta_group"]) == (2, 2, 128, 4, 1)
+    assert (p["tiles_m"], p["tiles_n"], p["tile_m"], p["tile_n"], p["k_steps"], p["cta_group"], p["grid"]) == \
+        (2, 2, 128, 128, 2, 2, 8)
+    assert p["tmem_cols"] == 128
+    try:
+        tc.gemm_f16_set_config(cta_group=1)
+        p = tc.gemm_f16_plan(256, 256, 256, 0, num_sms=152)
+        assert (p["tiles_m"], p["tiles_n"], p["tile_n"], p["k_steps"], p["cta_group"]) == (2, 2, 128, 4, 1)
+    finally:
+        tc.gemm_f16_set_config()
+    # one-CTA tiles once the 128 x 128 tiles outnumber the pairs
+    p = tc.gemm_f16_plan(1280, 1024, 256, 0, num_sms=152)
+    assert (p["cta_group"], p["tile_m"], p["num_tiles"], p["grid"]) == (1, 128, 80, 80)
     # the big square problem takes 256 x 256 tiles on CTA pairs
     p = tc.gemm_f16_plan(8192, 8192, 8192, 0, num_sms=152)
     assert (p["cta_group"], p["tile_m"], p["tile_n"], p["num_tiles"], p["grid"]) == (2, 256, 256, 1024, 152)
@@ -151,8 +165,15 @@ def test_cta_pair_planning(lib):
             tc.gemm_f16_plan(256, 256, 0, 0, num_sms=152)
         with pytest.raises(tc.GemmError):
             tc.gemm_f16_set_config(cta_group=2, split=2)
+        tc.gemm_f16_set_config(cta_group=2, tile_n=128)      # 128 x 128 pair tiles, 128-deep steps
+        p = tc.gemm_f16_plan(600, 520, 776, 0, num_sms=152)
+        assert (p["tile_m"], p["tile_n"], p["tile_k"], p["tiles_m"], p["tiles_n"], p["grid"]) == \
+            (128, 128, 128, 5, 5, 50)
+        tc.gemm_f16_set_config(cta_group=2, tile_n=128, tile_k=64)
         with pytest.raises(tc.GemmError):
-            tc.gemm_f16_set_config(cta_group=2, tile_n=128)
+            tc.gemm_f16_plan(600, 520, 776, 0, num_sms=152)
+        with pytest.raises(tc.GemmError):
+            tc.gemm_f16_set_config(cta_group=2, tile_n=64)
         with pytest.raises(tc.GemmError):
             tc.gemm_f16_set_config(cta_group=3)
         tc.gemm_f16_set_config(cta_group=2, grid=4)
@@ -217,10 +238,19 @@ def test_split_k_planning(lib):
 
 
 def test_plan_ragged_and_degenerate(lib):
+    # small problems: 128 x 128 tiles on CTA pairs with 128-deep steps
     p = tc.gemm_f16_plan(300, 392, 520, 0, num_sms=152)
-    assert (p["tiles_m"], p["tiles_n"], p["k_steps"]) == (3, 4, 9)
+    assert (p["cta_group"], p["tiles_m"], p["tiles_n"], p["k_steps"], p["grid"]) == (2, 3, 4, 5, 24)
     p = tc.gemm_f16_plan(1, 8, 8, 1, num_sms=152)
-    assert (p["num_tiles"], p["k_steps"], p["grid"]) == (1, 1, 1)
+    assert (p["num_tiles"], p["k_steps"], p["grid"]) == (1, 1, 2)
+    try:
+        tc.gemm_f16_set_config(cta_group=1)
+        p = tc.gemm_f16_plan(300, 392, 520, 0, num_sms=152)
+        assert (p["tiles_m"], p["tiles_n"], p["k_steps"]) == (3, 4, 9)
+        p = tc.gemm_f16_plan(1, 8, 8, 1, num_sms=152)
+        assert (p["num_tiles"], p["k_steps"], p["grid"]) == (1, 1, 1)
+    finally:
+        tc.gemm_f16_set_config()
     p = tc.gemm_f16_plan(128, 128, 0, 0, num_sms=152)
     assert p["k_steps"] == 0 and p["num_tiles"] == 1
 
@@ -230,10 +260,14 @@ def test_stages_clamp_and_release_rule(lib):
     ring holds stages + release buffers.  stages is clamped to the steps one
     CTA runs and must exceed release, as emit_pipeline requires."""
     try:
+        p = tc.gemm_f16_plan(128, 128, 256, 0, num_sms=152)  # one small pair tile: 2 steps of 128
+        assert (p["cta_group"], p["stages"], p["slots"]) == (2, 2, 2)
+        tc.gemm_f16_set_config(cta_group=1)
         p = tc.gemm_f16_plan(128, 128, 128, 0, num_sms=152)  # 2 steps, 1 tile
         assert (p["stages"], p["slots"]) == (2, 2)
         p = tc.gemm_f16_plan(128, 128, 64, 0, num_sms=152)   # 1 step
         assert (p["stages"], p["slots"]) == (1, 1)
+        tc.gemm_f16_set_config()
         p = tc.gemm_f16_plan(4096, 4096, 4096, 0, num_sms=152)   # CTA pairs: 64 KiB steps
         assert (p["cta_group"], p["stages"], p["release"], p["slots"]) == (2, 3, 0, 3)
         tc.gemm_f16_set_config(cta_group=1)

@@ -41,7 +41,8 @@ def same_bits(x, y):
 CHAINS = {
     "pairs_stream_k": (4096, 4096, 4096, 4096),  # CTA pairs with a stream-K tail, twice
     "split_k_twice": (128, 8192, 8192, 2048),    # skinny split-K, then a split-K product of its output
-    "one_cta_tiles": (640, 520, 1032, 776),      # ragged one-CTA tiles, twice
+    "small_pair_tiles": (640, 520, 1032, 776),   # ragged 128 x 128 tiles on CTA pairs, twice
+    "one_cta_then_pair": (1280, 256, 1024, 512),  # 80 one-CTA tiles, then 40 small pair tiles
 }
 
 

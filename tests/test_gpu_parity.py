@@ -114,14 +114,18 @@ def test_split_k(split, tile_n, out_dtype):
 
 
 PAIR_VARIANTS = ([dict(cta_group=2, tile_k=64, stages=s, release=r) for s, r in [(1, 0), (2, 1), (3, 0), (4, 2), (6, 0)]]
-                 + [dict(cta_group=2, tile_k=128, stages=s, release=r) for s, r in [(1, 0), (2, 1), (3, 0)]])
+                 + [dict(cta_group=2, tile_k=128, stages=s, release=r) for s, r in [(1, 0), (2, 1), (3, 0)]]
+                 + [dict(cta_group=2, tile_n=128, stages=s, release=r) for s, r in [(1, 0), (2, 1), (3, 0), (4, 2),
+                                                                                   (6, 0)]])
 
 
 @pytest.mark.parametrize("cfg", PAIR_VARIANTS,
-                         ids=lambda c: f"pair_k{c.get('tile_k', 64)}_s{c['stages']}r{c['release']}")
+                         ids=lambda c: f"pair{c.get('tile_n', 256)}_k{c.get('tile_k', 128 if 'tile_n' in c else 64)}"
+                                       f"_s{c['stages']}r{c['release']}")
 def test_cta_pair_variants(cfg):
-    """256 x 256 tiles on a CTA pair (cta_group::2): ragged M (half a pair
-    tile past the edge), N and K, every ring depth and release depth."""
+    """Tiles on a CTA pair (cta_group::2), 256 x 256 (128 rows per SM) and
+    128 x 128 (64 rows per SM, folded over the TMEM lanes): ragged M (half a
+    pair tile past the edge), N and K, every ring depth and release depth."""
     tc.gemm_f16_set_config(**cfg)
     a, b = make_inputs(600, 520, 776, ("uniform", 1.0), ("uniform", 1.0), seed_a=7, seed_b=8)
     for out_dtype in (0, 1):
@@ -142,6 +146,26 @@ def test_cta_pair_persistent_and_tiny():
         check_full(a, b, 1, f"pair tiny, step {tk}")
 
 
+def test_small_pair_tiles_persistent_and_exact():
+    """128 x 128 pair tiles: four pairs walk 54 tiles (both TMEM accumulators
+    wrap many times); all-ones and identity products are exact bit for bit."""
+    tc.gemm_f16_set_config(cta_group=2, tile_n=128, grid=8, raster_group=3)
+    plan = tc.gemm_f16_plan(1100, 760, 600, 0)
+    assert (plan["tile_m"], plan["tile_n"], plan["num_tiles"], plan["grid"]) == (128, 128, 54, 8)
+    a, b = make_inputs(1100, 760, 600, ("normal", 1.0), ("normal", 1.0), seed_a=41, seed_b=42)
+    check_full(a, b, 0, "small pair tiles, persistent")
+    tc.gemm_f16_set_config(cta_group=2, tile_n=128)
+    ones_a = torch.ones((200, 32768), dtype=torch.float16, device="cuda")
+    ones_b = torch.ones((32768, 136), dtype=torch.float16, device="cuda")
+    c = tc.matmul(ones_a, ones_b, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert bool((c == 32768).all())
+    x, _ = make_inputs(190, 8, 264, ("uniform", 1.0), ("uniform", 1.0), seed_a=43, seed_b=44)
+    eye = torch.eye(264, dtype=torch.float16)
+    c = gpu_gemm(x, eye, 0)
+    assert torch.equal(c.view(torch.int16), x.view(torch.int16))
+
+
 def ws_gemm(a, b, out_dtype, ws):
     a_d, b_d = a.cuda(), b.cuda()
     c = tc.matmul(a_d, b_d, out_dtype=torch.float16 if out_dtype == 0 else torch.float32, workspace=ws)
@@ -149,12 +173,14 @@ def ws_gemm(a, b, out_dtype, ws):
     return c.cpu()
 
 
+@pytest.mark.parametrize("tile_n", [256, 128])
 @pytest.mark.parametrize("grid", [0, 10])
 @pytest.mark.parametrize("out_dtype", [0, 1])
-def test_stream_k_every_tile_shared(grid, out_dtype):
+def test_stream_k_every_tile_shared(tile_n, grid, out_dtype):
     """stream_k 2: every tile's K iterations are shared by several pairs
-    (owner plus up to four contributors per tile), ragged M, N and K."""
-    tc.gemm_f16_set_config(cta_group=2, stream_k=2, grid=grid)
+    (owner plus contributors per tile), ragged M, N and K, on 256 x 256 and
+    128 x 128 pair tiles."""
+    tc.gemm_f16_set_config(cta_group=2, stream_k=2, grid=grid, tile_n=tile_n)
     plan = tc.gemm_f16_plan(1100, 1280, 2056, out_dtype, with_workspace=True)
     assert plan["sk_tiles"] == plan["num_tiles"] and plan["dp_tiles"] == 0
     ws = tc.workspace(1100, 1280, 2056, out_dtype)
