@@ -444,7 +444,8 @@ def run_ours(args, w, dist: Dist):
     if dist.rank == 0:
         roofline = gemm_roofline(w, avg_launch_s)
         roofline["traffic"] = recorded_traffic(w.name, plan)
-        roofline["kernel"] = (f"gemm_f16_pair_kernel<{w.out_dtype},{plan['tile_k']}>" if plan["cta_group"] == 2
+        roofline["kernel"] = (f"gemm_f16_pair_kernel<{w.out_dtype},{plan['tile_k']},{plan['tile_m']},{plan['tile_n']}>"
+                              if plan["cta_group"] == 2
                               else f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>")
         roofline["avg_launch_ms"] = avg_launch_s * 1e3
         cpu = None
