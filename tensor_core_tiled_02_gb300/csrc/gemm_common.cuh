@@ -226,9 +226,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // to the warp's staging buffer in the 128-byte swizzle the C tensor map
 // expects (16-byte chunk j of row `lane` at chunk j ^ (lane % 8)), fence for
 // the async proxy and TMA-store it.  Staging is double-buffered per warp.
+// dry: everything but the store (the staging buffer is rewritten later).
 template <int OUT>
 __device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 32], const CUtensorMap* tmC,
-                                            uint32_t staging, int& nstore, int lane, int x, int y) {
+                                            uint32_t staging, int& nstore, int lane, int x, int y,
+                                            bool dry = false) {
     const uint32_t stg = staging + (uint32_t)((nstore & 1) * 4096);
     // the store issued from this buffer two rounds ago must have read it
     if (lane == 0) ptx::bulk_wait_group_read<1>();
@@ -252,6 +254,7 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
+    if (dry) return;
     if (lane == 0) {
         ptx::tma_store_2d(tmC, stg, x, y);
         ptx::bulk_commit_group();

@@ -268,6 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wcol = PM == 256 ? 0 : (q >> 1) * (PN / 2);
         int tl = 0;
         int nstore = 0;
+        // every pair holds at most one tile, with no stream-K units
+        const bool one_unit = p.sk_tiles == 0 && p.dp_tiles <= clusters;
         UnitIter u;
         unit_iter_init(u, p, cluster, clusters);
         int t, k0, k1;
@@ -324,16 +326,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                     prefetched = true;
                 }
             }
-            if (KB > 0) {
-                if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane))
-                    break;
-                ptx::tc_fence_after();
-            }
             const int row0 = mb * PM + (int)rank * L::kRows + wrow;
             const int col0 = nb * PN + wcol;
-            const uint32_t trow = lane_base + (uint32_t)(acc * L::kAccCols);
-
+            // A pair with a single tile (small problems) first runs the drain
+            // once dry, while its main loop runs: from the spare accumulator
+            // (never written then), into this warp's staging, with no store and
+            // no hand-back.  The real pass, on the critical path, then finds the
+            // code in the instruction cache: the first run of each stretch of
+            // it otherwise misses, ~500 cycles a time.
+            bool failed = false;
+#pragma unroll 1
+            for (int pass = (one_unit && tl == 1 && KB > 0) ? 0 : 1; pass < 2; ++pass) {
+                const bool dry = pass == 0;
+                if (KB > 0 && !dry) {
+                    if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull,
+                                   lane)) {
+                        failed = true;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                }
+                if (!dry && k0 > 0) break;  // stream-K contributor: parks its partial below
+                const uint32_t trow = lane_base + (uint32_t)((dry ? acc ^ 1 : acc) * L::kAccCols);
+#pragma unroll 1
+                for (int c = 0; c < L::kAccCols / kCols; ++c) {
+                    uint32_t v[kCols];
+                    if (KB > 0) {
+                        ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                        if constexpr (OUT == 0)
+                            ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                        ptx::tmem_ld_wait();
+                        if (!dry && c == L::kAccCols / kCols - 1) {
+                            // this CTA's half of the accumulator is read: tell the leader
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
+                    }
+                    // stream-K owner: add the contributors' partials (summed in cluster
+                    // order), from the spare accumulator or straight from the workspace
+                    if (prefetched) {
+                        uint32_t x[kCols];
+                        const uint32_t sp = lane_base + (uint32_t)((acc ^ 1) * L::kAccCols + c * kCols);
+                        ptx::tmem_ld_32x32b_x32(sp, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+                        if constexpr (OUT == 0) ptx::tmem_ld_32x32b_x32(sp + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+                        ptx::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
+                    }
+                    for (int qq = cluster + 1; !prefetched && qq < q_end; ++qq) {
+                        const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
+                        uint32_t x[kCols];
+#pragma unroll
+                        for (int j = 0; j < kCols / 4; ++j)
+                            ptx::ld_global_cg_v4(slot + (size_t)(((c * (kCols / 4) + j) * kBM + row_in_tile) * 4),
+                                                 x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+#pragma unroll
+                        for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
+                    }
+                    add_c_in<OUT>(v, p, row0 + lane, col0 + c * kCols);
+                    store_chunk<OUT>(v, &tmC, staging, nstore, lane, col0 + c * kCols, row0, dry);
+                    if (dry) break;  // one chunk runs all of the loop's code
+                }
+            }
+            if (failed) break;
             if (k0 > 0) {
+                const uint32_t trow = lane_base + (uint32_t)(acc * L::kAccCols);
                 // stream-K contributor: park this CTA's partial in the cluster's
                 // workspace slot as [TMEM column / 4][TMEM lane] 16-byte groups
                 // (consecutive lanes, consecutive 16 bytes), then release the flag
@@ -355,48 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) ptx::st_release_gpu(p.flags + (cluster * 2 + (int)rank) * 4 + q, p.epoch);
                 continue;
-            }
-#pragma unroll 1
-            for (int c = 0; c < L::kAccCols / kCols; ++c) {
-                uint32_t v[kCols];
-                if (KB > 0) {
-                    ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                    if constexpr (OUT == 0)
-                        ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                    ptx::tmem_ld_wait();
-                    if (c == L::kAccCols / kCols - 1) {
-                        // this CTA's half of the accumulator is read: tell the leader
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
-                }
-                // stream-K owner: add the contributors' partials (summed in cluster
-                // order), from the spare accumulator or straight from the workspace
-                if (prefetched) {
-                    uint32_t x[kCols];
-                    const uint32_t sp = lane_base + (uint32_t)((acc ^ 1) * L::kAccCols + c * kCols);
-                    ptx::tmem_ld_32x32b_x32(sp, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
-                    if constexpr (OUT == 0) ptx::tmem_ld_32x32b_x32(sp + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
-                    ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
-                }
-                for (int qq = cluster + 1; !prefetched && qq < q_end; ++qq) {
-                    const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
-                    uint32_t x[kCols];
-#pragma unroll
-                    for (int j = 0; j < kCols / 4; ++j)
-                        ptx::ld_global_cg_v4(slot + (size_t)(((c * (kCols / 4) + j) * kBM + row_in_tile) * 4),
-                                             x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
-                }
-                add_c_in<OUT>(v, p, row0 + lane, col0 + c * kCols);
-                store_chunk<OUT>(v, &tmC, staging, nstore, lane, col0 + c * kCols, row0);
             }
         }
         if (lane == 0) ptx::bulk_wait_group_read<0>();
