@@ -286,6 +286,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tl = 0;
         int nstore = 0;
         bool arrived = false;
+        // The first pass through the code that drains an accumulator misses the
+        // instruction cache, ~500 cycles a stretch, on the critical path of a
+        // small problem.  So when every CTA (under split-K every cluster) holds
+        // a single tile, the epilogue runs that code once dry while the main loop
+        // runs.  Under split-K over two ranks the dry pass writes this CTA's
+        // staging, which the partner pushes into: each rank arrives on the
+        // other's `red_ready` once its dry pass is done, and waits on its own
+        // before pushing (long done by then).
+        const bool dry_ok = has_k && ((split == 1 && p.sk_tiles == 0 && p.dp_tiles <= clusters) ||
+                                      (split == 2 && kPushToStaging));
         UnitIter u;
         unit_iter_init(u, p, cl, clusters);
         int t, k0, k1;
@@ -296,169 +306,207 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
-            if (has_k) {
-                // a legitimate wait here spans a whole tile's main loop: allow 4x
-                if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane))
-                    break;
-                ptx::tc_fence_after();
-            }
-            const int row0 = mb * kBM + q * 32;
-            const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-
-            if (split == 2) {
-                const uint32_t peer = rank ^ 1u;
-                if constexpr (!kPushToStaging) {
-                    // this CTA's MMAs are done, so its ring is idle: the partner may push
-                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, peer));
-                    if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane))
+            // Dry pass first (see dry_ok): everything the code below does once
+            // the accumulator is ready, on the other accumulator, with no store,
+            // no push and no hand-back; the real pass then finds the code in the
+            // instruction cache.
+            bool failed = false;
+#pragma unroll 1
+            for (int pass = (dry_ok && tl == 1) ? 0 : 1; pass < 2; ++pass) {
+                const bool dry = pass == 0;
+                if (has_k && !dry) {
+                    // a legitimate wait here spans a whole tile's main loop: allow 4x
+                    if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane)) {
+                        failed = true;
                         break;
-                }
-                // this warp's rows of the partner's chunks: TMEM -> registers -> the
-                // partner (consecutive lanes, consecutive 16 bytes)
-#pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
-                    if (c % 2 == (int)rank) continue;
-#pragma unroll 1
-                    for (int h = 0; h < kCols / 32; ++h) {
-                        uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(trow + c * kCols + h * 32, v);
-                        ptx::tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            ptx::st_async_v4(ptx::mapa(push_slot(c, q) + (uint32_t)(((h * 8 + j) * 32 + lane) * 16), peer),
-                                             v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
-                                             ptx::mapa(red_data_bar, peer));
                     }
+                    ptx::tc_fence_after();
                 }
-                // the partner's blocks of this CTA's chunks
-                if (owned > 0 &&
-                    !warp_wait<true>(red_data_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceData, lane))
-                    break;
-                // done with the partner: its pushes have landed here, and it arrives
-                // only once this CTA's pushes have landed there
-                ptx::cluster_arrive();
-                arrived = true;
-            } else if (split > 2) {
-                // park the partial of every chunk another rank owns in this CTA's
-                // ring: this warp's 32 rows as [column / 4][row] 16-byte groups
+                const int row0 = mb * kBM + q * 32;
+                // the dry pass reads the other accumulator, which a CTA holding one tile never writes
+                const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)((dry ? acc ^ 1 : acc) * BN);
+
+                if (split == 2) {
+                    const uint32_t peer = rank ^ 1u;
+                    if constexpr (!kPushToStaging) {
+                        // this CTA's MMAs are done, so its ring is idle: the partner may push
+                        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, peer));
+                        if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane)) {
+                            failed = true;
+                            break;
+                        }
+                    } else if (!dry) {
+                        // the partner's dry pass, which wrote its staging, is done
+                        if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane)) {
+                            failed = true;
+                            break;
+                        }
+                    }
+                    // this warp's rows of the partner's chunks: TMEM -> registers -> the
+                    // partner (consecutive lanes, consecutive 16 bytes)
 #pragma unroll 1
-                for (int c = 0; c < kChunks; ++c) {
-                    if (c % split == (int)rank) continue;
+                    for (int c = 0; c < kChunks; ++c) {
+                        if (c % 2 == (int)rank) continue;
 #pragma unroll 1
-                    for (int h = 0; h < kCols / 32; ++h) {
+                        for (int h = 0; h < kCols / 32; ++h) {
+                            uint32_t v[32];
+                            ptx::tmem_ld_32x32b_x32(trow + c * kCols + h * 32, v);
+                            ptx::tmem_ld_wait();
+                            if (dry) continue;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                ptx::st_async_v4(ptx::mapa(push_slot(c, q) + (uint32_t)(((h * 8 + j) * 32 + lane) * 16), peer),
+                                                 v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3],
+                                                 ptx::mapa(red_data_bar, peer));
+                        }
+                    }
+                    // the partner's blocks of this CTA's chunks
+                    if (!dry && owned > 0 &&
+                        !warp_wait<true>(red_data_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceData, lane)) {
+                        failed = true;
+                        break;
+                    }
+                    // done with the partner: its pushes have landed here, and it arrives
+                    // only once this CTA's pushes have landed there
+                    if (!dry) {
+                        ptx::cluster_arrive();
+                        arrived = true;
+                    }
+                } else if (split > 2) {
+                    // park the partial of every chunk another rank owns in this CTA's
+                    // ring: this warp's 32 rows as [column / 4][row] 16-byte groups
+#pragma unroll 1
+                    for (int c = 0; c < kChunks; ++c) {
+                        if (c % split == (int)rank) continue;
+#pragma unroll 1
+                        for (int h = 0; h < kCols / 32; ++h) {
+                            uint32_t v[32];
+                            ptx::tmem_ld_32x32b_x32(trow + c * kCols + h * 32, v);
+                            ptx::tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                ptx::st_shared_v4(park_at(c, q) + (uint32_t)(((h * 8 + j) * 32 + lane) * 16), v[4 * j],
+                                                  v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int r = 0; r < split; ++r)
+                            if (r != (int)rank) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, (uint32_t)r));
+                    if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane)) {
+                        failed = true;
+                        break;
+                    }
+                } else if (k0 > 0) {
+                    // stream-K contributor: park this CTA's partial in its workspace
+                    // slot as [column / 4][row] 16-byte groups (consecutive lanes,
+                    // consecutive 16 bytes), then release this warp's flag
+                    float* slot = p.ws + (size_t)cl * kPartialFloats;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 32; ++c) {
                         uint32_t v[32];
-                        ptx::tmem_ld_32x32b_x32(trow + c * kCols + h * 32, v);
+                        ptx::tmem_ld_32x32b_x32(trow + c * 32, v);
                         ptx::tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
-                            ptx::st_shared_v4(park_at(c, q) + (uint32_t)(((h * 8 + j) * 32 + lane) * 16), v[4 * j],
+                            ptx::st_global_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), v[4 * j],
                                               v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) ptx::st_release_gpu(p.flags + cl * 4 + q, p.epoch);
+                    continue;
                 }
-                __syncwarp();
-                if (lane == 0)
-                    for (int r = 0; r < split; ++r)
-                        if (r != (int)rank) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, (uint32_t)r));
-                if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane)) break;
-            } else if (k0 > 0) {
-                // stream-K contributor: park this CTA's partial in its workspace
-                // slot as [column / 4][row] 16-byte groups (consecutive lanes,
-                // consecutive 16 bytes), then release this warp's flag
-                float* slot = p.ws + (size_t)cl * kPartialFloats;
-#pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld_32x32b_x32(trow + c * 32, v);
-                    ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        ptx::st_global_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), v[4 * j],
-                                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                // stream-K owner: the CTAs after this one whose shares start inside
+                // this tile hold the rest of its K range
+                int q_end = cl + 1;
+                if (split == 1 && k1 < p.k_blocks) {
+                    const long long tile_end = (long long)(t - p.dp_tiles + 1) * p.k_blocks;
+                    while (q_end < p.sk_pairs && sk_begin(p, q_end) < tile_end) ++q_end;
+                    bool ok = true;
+                    for (int qq = cl + 1; ok && qq < q_end; ++qq) {
+                        const unsigned* f = p.flags + qq * 4 + q;
+                        int r = 1;
+                        if (lane == 0) r = wait_flag(f, p.epoch, abort_flag, 4 * p.wait_limit);
+                        ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+                        if (ok) (void)ptx::ld_acquire_gpu(f);  // orders this lane's reads after the flag
+                    }
+                    if (!ok) {
+                        failed = true;
+                        break;
+                    }
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) ptx::st_release_gpu(p.flags + cl * 4 + q, p.epoch);
-                continue;
-            }
-            // stream-K owner: the CTAs after this one whose shares start inside
-            // this tile hold the rest of its K range
-            int q_end = cl + 1;
-            if (split == 1 && k1 < p.k_blocks) {
-                const long long tile_end = (long long)(t - p.dp_tiles + 1) * p.k_blocks;
-                while (q_end < p.sk_pairs && sk_begin(p, q_end) < tile_end) ++q_end;
-                bool ok = true;
-                for (int qq = cl + 1; ok && qq < q_end; ++qq) {
-                    const unsigned* f = p.flags + qq * 4 + q;
-                    int r = 1;
-                    if (lane == 0) r = wait_flag(f, p.epoch, abort_flag, 4 * p.wait_limit);
-                    ok = __shfl_sync(0xffffffffu, r, 0) != 0;
-                    if (ok) (void)ptx::ld_acquire_gpu(f);  // orders this lane's reads after the flag
-                }
-                if (!ok) break;
-            }
 
 #pragma unroll 1
-            for (int c = 0; c < BN / kCols; ++c) {
-                if (split > 1 && c % split != (int)rank) continue;
-                uint32_t v[kCols];
-                if (has_k) {
-                    ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                    if constexpr (OUT == 0)
-                        ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                    ptx::tmem_ld_wait();
-                    if (split == 1 && c == BN / kCols - 1) {
-                        // accumulator fully read: hand it back to the MMA warp
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+                for (int c = 0; c < BN / kCols; ++c) {
+                    if (split > 1 && c % split != (int)rank) continue;
+                    uint32_t v[kCols];
+                    if (has_k) {
+                        ptx::tmem_ld_32x32b_x32(trow + c * kCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                        if constexpr (OUT == 0)
+                            ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                        ptx::tmem_ld_wait();
+                        if (!dry && split == 1 && c == BN / kCols - 1) {
+                            // accumulator fully read: hand it back to the MMA warp
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
                     }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
-                }
-                if (split == 2) {
-                    // the partner's partial, pushed into this CTA
-                    uint32_t x[kCols];
-#pragma unroll
-                    for (int j = 0; j < kCols / 4; ++j)
-                        ptx::ld_shared_v4(push_slot(c, q) + (uint32_t)((j * 32 + lane) * 16), x[4 * j], x[4 * j + 1],
-                                          x[4 * j + 2], x[4 * j + 3]);
-                    // every lane has its values before any lane reuses the staging
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
-                } else if (split > 2) {
-                    // add the other ranks' partials to this rank's own, in ascending
-                    // rank order: a fixed order, so the result is deterministic
-                    for (int r = 0; r < split; ++r) {
-                        if (r == (int)rank) continue;
-                        // all of the chunk's remote loads in flight at once, then the adds
+                    if (split == 2) {
+                        // the partner's partial, pushed into this CTA
                         uint32_t x[kCols];
 #pragma unroll
                         for (int j = 0; j < kCols / 4; ++j)
-                            ptx::ld_cluster_v4(ptx::mapa(park_at(c, q) + (uint32_t)((j * 32 + lane) * 16), (uint32_t)r),
-                                               x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+                            ptx::ld_shared_v4(push_slot(c, q) + (uint32_t)((j * 32 + lane) * 16), x[4 * j], x[4 * j + 1],
+                                              x[4 * j + 2], x[4 * j + 3]);
+                        // every lane has its values before any lane reuses the staging
+                        __syncwarp();
+#pragma unroll
+                        for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
+                    } else if (split > 2) {
+                        // add the other ranks' partials to this rank's own, in ascending
+                        // rank order: a fixed order, so the result is deterministic
+                        for (int r = 0; r < split; ++r) {
+                            if (r == (int)rank) continue;
+                            // all of the chunk's remote loads in flight at once, then the adds
+                            uint32_t x[kCols];
+#pragma unroll
+                            for (int j = 0; j < kCols / 4; ++j)
+                                ptx::ld_cluster_v4(ptx::mapa(park_at(c, q) + (uint32_t)((j * 32 + lane) * 16), (uint32_t)r),
+                                                   x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+#pragma unroll
+                            for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
+                        }
+                    }
+                    // stream-K owner: add the contributors' partials, in CTA order
+                    for (int qq = cl + 1; qq < q_end; ++qq) {
+                        const float* slot = p.ws + (size_t)qq * kPartialFloats;
+                        uint32_t x[kCols];
+#pragma unroll
+                        for (int j = 0; j < kCols / 4; ++j)
+                            ptx::ld_global_cg_v4(slot + (size_t)(((c * (kCols / 4) + j) * kBM + row_in_tile) * 4),
+                                                 x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
 #pragma unroll
                         for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                     }
+                    add_c_in<OUT>(v, p, row0 + lane, nb * BN + c * kCols);
+                    store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, row0, dry);
+                    if (dry) break;  // one chunk runs all of the loop's code
                 }
-                // stream-K owner: add the contributors' partials, in CTA order
-                for (int qq = cl + 1; qq < q_end; ++qq) {
-                    const float* slot = p.ws + (size_t)qq * kPartialFloats;
-                    uint32_t x[kCols];
-#pragma unroll
-                    for (int j = 0; j < kCols / 4; ++j)
-                        ptx::ld_global_cg_v4(slot + (size_t)(((c * (kCols / 4) + j) * kBM + row_in_tile) * 4),
-                                             x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
-#pragma unroll
-                    for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
+                // split-K over two ranks: this CTA's staging is the partner's to push into
+                if (dry && split == 2) {
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, rank ^ 1u));
                 }
-                add_c_in<OUT>(v, p, row0 + lane, nb * BN + c * kCols);
-                store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, row0);
             }
+            if (failed) break;
         }
         // after an abort: bytes the partner may still push land before this CTA leaves
         if (split == 2 && owned > 0 && warp == 2 && lane == 0) wait_drain(red_data_bar, 0, p.wait_limit);
