@@ -155,6 +155,9 @@ size_t flag_bytes_for(int ctas) { return ((size_t)ctas * 4 * sizeof(unsigned) + 
 size_t workspace_for(int ctas) { return flag_bytes_for(ctas) + (size_t)ctas * kPartialFloats * sizeof(float); }
 
 // The planner.
+// CTA pairs with 256 x 256 tiles for large problems (see the cta_group choice
+// below); CTA pairs with 128 x 128 tiles for small ones whose tiles fit one
+// wave of pairs without splitting K.  Otherwise one CTA per tile:
 // Tile: 128 x 256 or 128 x 128, whichever needs less time counted in waves of
 // tiles over the SMs, a 128 x 128 tile costing 0.85 of a 128 x 256 one (half
 // the MMA work at about 0.6 of the tensor-pipe efficiency, measured: it needs
