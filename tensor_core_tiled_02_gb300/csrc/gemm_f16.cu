@@ -35,8 +35,9 @@ struct DeviceInfo {
     int sms = 0;
     int cc = 0;
     std::atomic<int> max_pairs{0};  // CTA-pair clusters the GPU holds at once (0: not yet asked)
-    // [tile_n 64 / 128 / 256, CTA pair step K 64 / 128, blocked add][out_dtype]: the
-    // kernel's shared-memory limit has been raised on this device
+    // [tile_n 64 / 128 / 256, 256 x 256 CTA pair with step K 64 / 128, blocked add,
+    // 128 x 128 CTA pair][out_dtype]: the kernel's shared-memory limit has been
+    // raised on this device
     std::atomic<bool> attr_set[7][2];
 };
 DeviceInfo g_dev[kMaxDevices];  // static storage: every atomic starts zero
