@@ -35,6 +35,8 @@ struct DeviceInfo {
     int sms = 0;
     int cc = 0;
     std::atomic<int> max_pairs{0};  // CTA-pair clusters the GPU holds at once (0: not yet asked)
+    // [s]: clusters of s one-CTA-per-SM CTAs of the one-CTA kernel the GPU holds at once (0: not yet asked)
+    std::atomic<int> max_clusters[kMaxSplit + 1];
     // [tile_n 64 / 128 / 256, 256 x 256 CTA pair with step K 64 / 128, blocked add,
     // 128 x 128 CTA pair][out_dtype]: the kernel's shared-memory limit has been
     // raised on this device
@@ -155,6 +157,26 @@ size_t flag_bytes_for(int ctas) { return ((size_t)ctas * 4 * sizeof(unsigned) + 
 
 size_t workspace_for(int ctas) { return flag_bytes_for(ctas) + (size_t)ctas * kPartialFloats * sizeof(float); }
 
+// Clusters the GPU can hold at once, by cluster size (one CTA per SM): [1] the
+// SMs, [2] CTA pairs, [3 .. kMaxSplit] split-K clusters.  Not every size packs
+// the SMs: on a 152-SM GB300 they are 76, 46, 36, 28, 23, 15 and 15 clusters
+// of 2 .. 8 (a cluster's CTAs share a GPC).  A split-K launch whose clusters do
+// not all fit at once runs in two waves.
+struct Fit {
+    int clusters[kMaxSplit + 1];
+};
+
+// For planning without the device at hand: the 152-SM GB300 figures, scaled
+// to `num_sms`.
+Fit fit_estimate(int num_sms) {
+    static const int kGb300[kMaxSplit + 1] = {0, 152, 76, 46, 36, 28, 23, 15, 15};
+    Fit f;
+    f.clusters[0] = 0;
+    for (int c = 1; c <= kMaxSplit; ++c) f.clusters[c] = (int)((long long)kGb300[c] * num_sms / 152);
+    if (f.clusters[2] < 1 && num_sms >= 2) f.clusters[2] = 1;
+    return f;
+}
+
 // The planner.
 // CTA pairs with 256 x 256 tiles for large problems (see the cta_group choice
 // below); CTA pairs with 128 x 128 tiles for small ones whose tiles fit one
@@ -171,17 +193,34 @@ size_t workspace_for(int ctas) { return flag_bytes_for(ctas) + (size_t)ctas * kP
 // emit_pipeline, stages must exceed release, and stages is clamped to the
 // steps one CTA runs (never below release + 1).  Default: the deepest ring
 // that fits shared memory.
-int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bool with_workspace,
+int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, bool with_workspace,
               const gemm_config& cfg, gemm_plan* p) {
     std::memset(p, 0, sizeof(*p));
+    int max_pairs = fit.clusters[2];
     p->tile_m = kBM;
     p->tile_k = kBK;
     const int tiles_m = ceil_div(M, kBM);
     int tn = cfg.tile_n;
+    bool wide_to_split = false;
     if (tn == 0) {
-        const long long w256 = ((long long)tiles_m * ceil_div(N, 256) + num_sms - 1) / num_sms;
-        const long long w128 = ((long long)tiles_m * ceil_div(N, 128) + num_sms - 1) / num_sms;
+        const long long t256 = (long long)tiles_m * ceil_div(N, 256);
+        const long long t128 = (long long)tiles_m * ceil_div(N, 128);
+        const long long w256 = (t256 + num_sms - 1) / num_sms;
+        const long long w128 = (t128 + num_sms - 1) / num_sms;
         tn = w256 * 100 <= w128 * 85 ? 256 : 128;
+        // Each SM takes in at most about 100 GB/s of operands from L2, so a
+        // one-CTA tile's time goes with the bytes it loads: per K step 32 KiB
+        // for a 128 x 128 tile, 48 KiB for twice the work on 128 x 256.  When
+        // 128 x 128 tiles would fill more than half the SMs, and so run
+        // unsplit, but 128 x 256 tiles leave room to split K two ways, the wide
+        // split tiles load 3/4 of the bytes per CTA on as many CTAs:
+        // 512 x 4096 x 8192 measured 45.1 -> 31.6 us, 256 x 8192 x 8192 45.4
+        // -> 35.0 us (CTA pairs with a stream-K tail: 35.4 and 40.3 us).
+        if (tn == 128 && cfg.split == 0 && cfg.stream_k != 2 && 2 * t128 > num_sms && 2 * t256 <= num_sms &&
+            ceil_div(K, kBK) / 16 >= 2) {
+            tn = 256;
+            wide_to_split = true;
+        }
     }
     p->tile_n = tn;
     p->tiles_m = tiles_m;
@@ -197,7 +236,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bo
     if (cg == 0) {
         cg = 1;
         const long long tiles128 = (long long)tiles_m * ceil_div(N, 128);
-        if (tn == 256 && cfg.tile_n == 0 && cfg.split <= 1 && p->k_steps > 0 && num_sms >= 2) {
+        if (tn == 256 && !wide_to_split && cfg.tile_n == 0 && cfg.split <= 1 && p->k_steps > 0 && num_sms >= 2) {
             const long long pair_tiles = (long long)ceil_div(M, 2 * kBM) * ceil_div(N, 256);
             const long long w_pair = (pair_tiles + num_sms / 2 - 1) / (num_sms / 2);
             const long long w_one = ((long long)p->num_tiles + num_sms - 1) / num_sms;
@@ -327,6 +366,9 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, int max_pairs, bo
             split = num_sms / p->num_tiles;
             if (split > kMaxSplit) split = kMaxSplit;
             if (split > p->k_steps / 16) split = p->k_steps / 16;
+            // every cluster resident at once (one wave): 48 clusters of three
+            // where 46 fit took 32.7 us at 768 x 2048 x 4096, split 2 ~half that
+            while (split > 1 && p->num_tiles > fit.clusters[split]) --split;
             if (split < 1) split = 1;
         }
     }
@@ -513,6 +555,46 @@ int max_pairs_of(DeviceInfo& dev) {
     return dev.max_pairs.load(std::memory_order_relaxed);
 }
 
+// Split-K clusters of `size` CTAs the GPU can hold at once (asked once per
+// device and size).
+int max_clusters_of(DeviceInfo& dev, int size) {
+    const int known = dev.max_clusters[size].load(std::memory_order_acquire);
+    if (known > 0) return known;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (dev.max_clusters[size].load(std::memory_order_relaxed) == 0) {
+        cudaLaunchConfig_t lc = {};
+        lc.gridDim = dim3((dev.sms / size) * size, 1, 1);
+        lc.blockDim = dim3(kThreads, 1, 1);
+        lc.dynamicSmemBytes = kSmemLimit;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = size;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        lc.attrs = attr;
+        lc.numAttrs = 1;
+        auto kern = gemm_f16_kernel<128, 0>;
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, kern, &lc) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = fit_estimate(dev.sms).clusters[size];
+            if (n < 1) n = 1;
+        }
+        dev.max_clusters[size].store(n, std::memory_order_release);
+    }
+    return dev.max_clusters[size].load(std::memory_order_relaxed);
+}
+
+Fit fit_of(DeviceInfo& dev) {
+    Fit f;
+    f.clusters[0] = 0;
+    f.clusters[1] = dev.sms;
+    f.clusters[2] = max_pairs_of(dev);
+    for (int c = 3; c <= kMaxSplit; ++c) f.clusters[c] = max_clusters_of(dev, c);
+    return f;
+}
+
 gemm_config current_config() {
     std::lock_guard<std::mutex> lk(g_mu);
     return g_cfg;
@@ -530,7 +612,7 @@ int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, 
     if (rc != GEMM_OK) return rc;
     if (dev->cc != 103) return GEMM_ERR_ARCH;
     gemm_plan plan;
-    rc = plan_impl(M, N, K, out_dtype, dev->sms, max_pairs_of(*dev), workspace != nullptr, cfg, &plan);
+    rc = plan_impl(M, N, K, out_dtype, dev->sms, fit_of(*dev), workspace != nullptr, cfg, &plan);
     if (rc != GEMM_OK) return rc;
     if (plan.sk_tiles > 0 && (size_t)plan.workspace_bytes > workspace_bytes) return GEMM_ERR_WORKSPACE;
 
@@ -606,15 +688,13 @@ int plan_entry(int M, int N, int K, int out_dtype, int num_sms, bool with_worksp
     int rc = check_args(nullptr, nullptr, nullptr, M, N, K, out_dtype, false);
     if (rc < 0) return rc;
     if (num_sms < 0) return GEMM_ERR_DIM;
-    int max_pairs = num_sms / 2;
     if (num_sms == 0) {
         DeviceInfo* dev = nullptr;
         rc = device_info(&dev);
         if (rc != GEMM_OK) return rc;
-        num_sms = dev->sms;
-        max_pairs = max_pairs_of(*dev);
+        return plan_impl(M, N, K, out_dtype, dev->sms, fit_of(*dev), with_workspace, current_config(), out);
     }
-    return plan_impl(M, N, K, out_dtype, num_sms, max_pairs, with_workspace, current_config(), out);
+    return plan_impl(M, N, K, out_dtype, num_sms, fit_estimate(num_sms), with_workspace, current_config(), out);
 }
 
 }  // namespace
@@ -835,7 +915,7 @@ extern "C" int gemm_f16_noalloc(const gemm_f16_t* A, const gemm_f16_t* B, void* 
     if (rc != GEMM_OK) return rc;
     if (dev->cc != 103) return GEMM_ERR_ARCH;
     gemm_plan plan;
-    rc = plan_impl(M, N, K, out_dtype, dev->sms, max_pairs_of(*dev), true, current_config(), &plan);
+    rc = plan_impl(M, N, K, out_dtype, dev->sms, fit_of(*dev), true, current_config(), &plan);
     if (rc != GEMM_OK) return rc;
     if (plan.sk_tiles > 0 && (size_t)plan.workspace_bytes > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
     void* scratch = nullptr;

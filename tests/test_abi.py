@@ -237,6 +237,37 @@ def test_split_k_planning(lib):
         tc.gemm_f16_set_config()
 
 
+# clusters of 1 .. 8 CTAs (one per SM) a 152-SM GB300 holds at once
+RESIDENT = {1: 152, 2: 76, 3: 46, 4: 36, 5: 28, 6: 23, 7: 15, 8: 15}
+
+
+def test_split_k_clusters_all_fit_at_once(lib):
+    """Split-K clusters must all be resident together (one wave); the split is
+    lowered until they are.  Spot checks, then an invariant over many shapes."""
+    p = tc.gemm_f16_plan(128, 2048, 8192, 0, num_sms=152)   # 16 tiles: 8 ranks would need 16 clusters of 8
+    assert (p["num_tiles"], p["split"], p["grid"]) == (16, 6, 96)
+    p = tc.gemm_f16_plan(768, 2048, 4096, 0, num_sms=152)   # 48 clusters of 3 would not fit: 2 ranks
+    assert (p["tile_n"], p["num_tiles"], p["split"], p["grid"]) == (256, 48, 2, 96)
+    for M in (64, 128, 256, 384, 512, 768, 1024, 1280):
+        for N in (256, 512, 1024, 2048, 4096, 8192):
+            for K in (2048, 8192, 32768):
+                p = tc.gemm_f16_plan(M, N, K, 0, num_sms=152)
+                if p["split"] > 1:
+                    assert p["num_tiles"] <= RESIDENT[p["split"]], (M, N, K, p)
+
+
+def test_wide_tiles_to_split_k(lib):
+    """128 x 128 tiles that would run unsplit on over half the SMs give way to
+    128 x 256 tiles split along K (each CTA loads 3/4 of the bytes)."""
+    p = tc.gemm_f16_plan(512, 4096, 8192, 0, num_sms=152)
+    assert (p["cta_group"], p["tile_n"], p["num_tiles"], p["split"], p["grid"]) == (1, 256, 64, 2, 128)
+    p = tc.gemm_f16_plan(256, 8192, 8192, 0, num_sms=152)
+    assert (p["cta_group"], p["tile_n"], p["num_tiles"], p["split"], p["grid"]) == (1, 256, 64, 2, 128)
+    # short K: nothing to split, the narrow tiles stay
+    p = tc.gemm_f16_plan(1280, 1024, 256, 0, num_sms=152)
+    assert (p["tile_n"], p["split"]) == (128, 1)
+
+
 def test_plan_ragged_and_degenerate(lib):
     # small problems: 128 x 128 tiles on CTA pairs with 128-deep steps
     p = tc.gemm_f16_plan(300, 392, 520, 0, num_sms=152)
