@@ -64,8 +64,8 @@ struct Layout {
     static constexpr int kStagingBytes = 32 * 128;       // one warp's 32 rows x 128 bytes
     static constexpr int kTmemCols = 2 * BN;             // two accumulators
     static constexpr int kPartialBytes = kBM * BN * 4;   // one fp32 partial tile (split-K)
-    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain, red_ready, red_data
-    static constexpr int kNumBars = 2 * kMaxStages + 7;
+    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain, red_ready, red_data, dry
+    static constexpr int kNumBars = 2 * kMaxStages + 8;
     static constexpr int kFixedBytes = 4 * 2 * kStagingBytes + kNumBars * 8 + 16;
     static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
 };
@@ -226,11 +226,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // to the warp's staging buffer in the 128-byte swizzle the C tensor map
 // expects (16-byte chunk j of row `lane` at chunk j ^ (lane % 8)), fence for
 // the async proxy and TMA-store it.  Staging is double-buffered per warp.
-// dry: everything but the store (the staging buffer is rewritten later).
+// skip_store: everything but the TMA store itself (and nstore stays).  A dry
+// pass through the drain normally stores instead to rows from M on, which
+// the tensor map clips entirely: no byte of C is written.
 template <int OUT>
 __device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 32], const CUtensorMap* tmC,
                                             uint32_t staging, int& nstore, int lane, int x, int y,
-                                            bool dry = false) {
+                                            bool skip_store = false) {
     const uint32_t stg = staging + (uint32_t)((nstore & 1) * 4096);
     // the store issued from this buffer two rounds ago must have read it
     if (lane == 0) ptx::bulk_wait_group_read<1>();
@@ -254,7 +256,7 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    if (dry) return;
+    if (skip_store) return;
     if (lane == 0) {
         ptx::tma_store_2d(tmC, stg, x, y);
         ptx::bulk_commit_group();

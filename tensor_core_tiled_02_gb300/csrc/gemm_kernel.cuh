@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
     const uint32_t red_ready_bar = bar0 + 8u * (2 * kMaxStages + 5);
     const uint32_t red_data_bar = bar0 + 8u * (2 * kMaxStages + 6);
+    const uint32_t dry_bar = bar0 + 8u * (2 * kMaxStages + 7);  // takes the dry drain's hand-back; never waited on
     // split-K parking: chunk c, epilogue warp quadrant q -> one contiguous
     // block of kCols / 4 column groups x 32 rows x 16 bytes in the ring
     constexpr int kChunks = BN / kCols;
@@ -135,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // red_data (split 2): this CTA's own expect-tx arrival plus the pushed bytes
         ptx::mbar_init(red_ready_bar, split > 1 ? 4 * (split - 1) : 1);
         ptx::mbar_init(red_data_bar, 1);
+        ptx::mbar_init(dry_bar, 4);
         // split 2: armed now for every byte the partner will push here
         if (split == 2 && owned > 0) ptx::mbar_arrive_expect_tx(red_data_bar, (uint32_t)owned * 4u * kWarpChunkBytes);
         *abort_flag = 0;
@@ -276,10 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (split > 1) ptx::cluster_arrive();
     } else {
         // ---------------- epilogue: TMEM -> registers -> SMEM -> TMA store ----------------
-        // the previous kernel's reads and writes of C (and of the workspace) are
-        // done from here on
-        ptx::grid_dependency_wait();
-        ptx::grid_launch_dependents();
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const uint32_t staging = sC + (uint32_t)(q * 2 * L::kStagingBytes);
         const int row_in_tile = q * 32 + lane;
@@ -289,13 +287,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The first pass through the code that drains an accumulator misses the
         // instruction cache, ~500 cycles a stretch, on the critical path of a
         // small problem.  So when every CTA (under split-K every cluster) holds
-        // a single tile, the epilogue runs that code once dry while the main loop
-        // runs.  Under split-K over two ranks the dry pass writes this CTA's
-        // staging, which the partner pushes into: each rank arrives on the
-        // other's `red_ready` once its dry pass is done, and waits on its own
-        // before pushing (long done by then).
+        // a single tile, the epilogue runs that code once dry, before the wait
+        // for the previous kernel and while the main loop runs: on the other
+        // accumulator, storing to rows from M on (clipped: no byte of C
+        // written), handing back on a barrier nobody waits on, pushing nothing.
+        // Under split-K over two ranks the dry pass writes this CTA's staging,
+        // which the partner pushes into: each rank arrives on the other's
+        // `red_ready` once its dry pass is done, and waits on its own before
+        // pushing (long done by then).
         const bool dry_ok = has_k && ((split == 1 && p.sk_tiles == 0 && p.dp_tiles <= clusters) ||
                                       (split == 2 && kPushToStaging));
+        if (!dry_ok) {
+            // the previous kernel's reads and writes of C (and of the workspace)
+            // are done from here on
+            ptx::grid_dependency_wait();
+            ptx::grid_launch_dependents();
+        }
         UnitIter u;
         unit_iter_init(u, p, cl, clusters);
         int t, k0, k1;
@@ -314,6 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int pass = (dry_ok && tl == 1) ? 0 : 1; pass < 2; ++pass) {
                 const bool dry = pass == 0;
+                if (dry_ok && !dry) {
+                    // the previous kernel's reads and writes of C are done from here on
+                    ptx::grid_dependency_wait();
+                    ptx::grid_launch_dependents();
+                }
                 if (has_k && !dry) {
                     // a legitimate wait here spans a whole tile's main loop: allow 4x
                     if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull, lane)) {
@@ -449,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (OUT == 0)
                             ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                         ptx::tmem_ld_wait();
-                        if (!dry && split == 1 && c == BN / kCols - 1) {
+                        if (split == 1 && c == BN / kCols - 1) {
                             // accumulator fully read: hand it back to the MMA warp
                             ptx::tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+                            if (lane == 0) ptx::mbar_arrive(dry ? dry_bar : tempty_bar(acc));
                         }
                     } else {
 #pragma unroll
@@ -496,9 +508,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                     }
-                    add_c_in<OUT>(v, p, row0 + lane, nb * BN + c * kCols);
-                    store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, row0, dry);
-                    if (dry) break;  // one chunk runs all of the loop's code
+                    add_c_in<OUT>(v, p, dry ? p.M : row0 + lane, nb * BN + c * kCols);  // row M: nothing read
+                    store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, dry ? p.M : row0,
+                                     dry && p.M > (1 << 30));
+                    if (dry) {
+                        // one chunk runs all of the loop's code; the staging is free
+                        // again and the real pass starts on buffer 0 (under split-K
+                        // the partner's pushed partials sit in both buffers)
+                        if (lane == 0) ptx::bulk_wait_group_read<0>();
+                        __syncwarp();
+                        nstore = 0;
+                        break;
+                    }
                 }
                 // split-K over two ranks: this CTA's staging is the partner's to push into
                 if (dry && split == 2) {

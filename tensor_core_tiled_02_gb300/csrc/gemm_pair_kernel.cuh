@@ -74,8 +74,8 @@ struct PairLayout {
     static constexpr int kStagingBytes = 32 * 128;
     static constexpr int kAccCols = PM == 256 ? PN : PN / 2;  // TMEM columns of one accumulator
     static constexpr int kTmemCols = 2 * kAccCols;            // two accumulators (256 x 256: all 512)
-    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain
-    static constexpr int kNumBars = 2 * kMaxStages + 5;
+    // full[8], empty[8], tmem_full[2], tmem_empty[2], drain, dry
+    static constexpr int kNumBars = 2 * kMaxStages + 6;
     static constexpr int kFixedBytes = 4 * 2 * kStagingBytes + kNumBars * 8 + 16;
     static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
 };
@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kMaxStages + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kMaxStages + 2 + a); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kMaxStages + 4);
+    const uint32_t dry_bar = bar0 + 8u * (2 * kMaxStages + 5);  // takes the dry drain's hand-back; never waited on
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -119,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(tempty_bar(a), 8);  // 4 epilogue warps in each CTA
         }
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(dry_bar, 8);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -256,10 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue (both CTAs): own PM/2 rows x PN columns ----------------
-        // the previous kernel's reads and writes of C and of the workspace are
-        // done from here on
-        ptx::grid_dependency_wait();
-        ptx::grid_launch_dependents();
         const int q = warp & 3;
         const uint32_t staging = sC + (uint32_t)(q * 2 * L::kStagingBytes);
         const int row_in_tile = q * 32 + lane;  // TMEM lane: the workspace's row index
@@ -270,6 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int nstore = 0;
         // every pair holds at most one tile, with no stream-K units
         const bool one_unit = p.sk_tiles == 0 && p.dp_tiles <= clusters;
+        // the dry pass (below) touches no byte of global memory, so it runs
+        // before the wait for the previous kernel; everything else after it
+        const bool dry_first = one_unit && KB > 0;
+        if (!dry_first) {
+            // the previous kernel's reads and writes of C and of the workspace
+            // are done from here on
+            ptx::grid_dependency_wait();
+            ptx::grid_launch_dependents();
+        }
         UnitIter u;
         unit_iter_init(u, p, cluster, clusters);
         int t, k0, k1;
@@ -329,15 +336,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = mb * PM + (int)rank * L::kRows + wrow;
             const int col0 = nb * PN + wcol;
             // A pair with a single tile (small problems) first runs the drain
-            // once dry, while its main loop runs: from the spare accumulator
-            // (never written then), into this warp's staging, with no store and
-            // no hand-back.  The real pass, on the critical path, then finds the
-            // code in the instruction cache: the first run of each stretch of
-            // it otherwise misses, ~500 cycles a time.
+            // once dry, before the wait for the previous kernel and while its
+            // main loop runs: from the spare accumulator (never written then),
+            // into this warp's staging, storing to rows from M on (clipped: no
+            // byte written), handing back on a barrier nobody waits on.  The real
+            // pass, on the critical path, then finds every instruction of it in
+            // the instruction cache: the first run of each stretch of code
+            // otherwise misses, ~500 cycles a time.
             bool failed = false;
 #pragma unroll 1
-            for (int pass = (one_unit && tl == 1 && KB > 0) ? 0 : 1; pass < 2; ++pass) {
+            for (int pass = (dry_first && tl == 1) ? 0 : 1; pass < 2; ++pass) {
                 const bool dry = pass == 0;
+                if (dry_first && !dry) {
+                    // the previous kernel's reads and writes of C are done from here on
+                    ptx::grid_dependency_wait();
+                    ptx::grid_launch_dependents();
+                }
                 if (KB > 0 && !dry) {
                     if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull,
                                    lane)) {
@@ -356,11 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (OUT == 0)
                             ptx::tmem_ld_32x32b_x32(trow + c * kCols + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
                         ptx::tmem_ld_wait();
-                        if (!dry && c == L::kAccCols / kCols - 1) {
+                        if (c == L::kAccCols / kCols - 1) {
                             // this CTA's half of the accumulator is read: tell the leader
                             ptx::tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
+                            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(dry ? dry_bar : tempty_bar(acc), 0));
                         }
                     } else {
 #pragma unroll
@@ -387,9 +401,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                     }
-                    add_c_in<OUT>(v, p, row0 + lane, col0 + c * kCols);
-                    store_chunk<OUT>(v, &tmC, staging, nstore, lane, col0 + c * kCols, row0, dry);
-                    if (dry) break;  // one chunk runs all of the loop's code
+                    add_c_in<OUT>(v, p, dry ? p.M : row0 + lane, col0 + c * kCols);  // row M: nothing read
+                    store_chunk<OUT>(v, &tmC, staging, nstore, lane, col0 + c * kCols, dry ? p.M : row0,
+                                     dry && p.M > (1 << 30));
+                    if (dry) {
+                        // one chunk runs all of the loop's code; the staging is free again
+                        if (lane == 0) ptx::bulk_wait_group_read<0>();
+                        __syncwarp();
+                        nstore = 0;
+                        break;
+                    }
                 }
             }
             if (failed) break;
