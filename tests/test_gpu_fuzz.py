@@ -4,7 +4,8 @@ Each case draws a ragged shape (N and K multiples of 8, as TMA needs) and
 one tuning configuration: one-CTA tiles of each width, split-K over a
 cluster, CTA pairs with 256 x 256 or 128 x 128 tiles, stream-K through a
 workspace, or the planner's own choice, with fp16 or fp32 output.  The
-whole product is compared element by element with the oracle.
+whole product is compared element by element with the oracle.  A second set
+accumulates into C's values (C += A B) the same way.
 """
 import numpy as np
 import pytest
@@ -12,7 +13,7 @@ import pytest
 import oracle
 import parity
 import tensor_core_tiled_02_gb300 as tc
-from tensor_core_tiled_02_gb300.synthetic import make_inputs
+from tensor_core_tiled_02_gb300.synthetic import draw, make_inputs
 
 torch = pytest.importorskip("torch")
 
@@ -77,3 +78,27 @@ def test_random_shape(M, N, K, cfg, out_dtype):
     torch.cuda.synchronize()
     ref = oracle.as_values(oracle.gemm(a.numpy(), b.numpy(), out_dtype), out_dtype)
     parity.check(c.cpu().double().numpy(), ref, K, out_dtype, f"{M}x{N}x{K} {cfg} plan {plan}")
+
+
+ACC_CASES = [draw_case(100 + i) for i in range(24)]
+
+
+@pytest.mark.parametrize("M,N,K,cfg,out_dtype", ACC_CASES,
+                         ids=[f"acc-{M}x{N}x{K}-{'-'.join(f'{k}{v}' for k, v in cfg.items()) or 'plan'}-o{o}"
+                              for M, N, K, cfg, o in ACC_CASES])
+def test_random_shape_accumulate(M, N, K, cfg, out_dtype):
+    """C += A B into C's values (gemm_f16_acc, no workspace) on the same kind
+    of random shapes and configurations."""
+    try:
+        tc.gemm_f16_set_config(**cfg)
+        tc.gemm_f16_plan(M, N, K, out_dtype)
+    except tc.GemmError:
+        tc.gemm_f16_set_config()
+    a, b = make_inputs(M, N, K, ("uniform", 1.0), ("uniform", 1.0), seed_a=M + 2 * K, seed_b=N + 3 * K)
+    c0 = draw((M, N), ("normal", 4.0), M + N)
+    c0 = c0 if out_dtype == 0 else c0.float()
+    c = c0.cuda()
+    tc.matmul_acc(a.cuda(), b.cuda(), c)
+    torch.cuda.synchronize()
+    ref = oracle.as_values(oracle.gemm_acc(a.numpy(), b.numpy(), c0.numpy(), out_dtype), out_dtype)
+    parity.check(c.cpu().double().numpy(), ref, K, out_dtype, f"accumulate {M}x{N}x{K} {cfg}")
