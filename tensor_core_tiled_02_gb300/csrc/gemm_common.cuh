@@ -115,6 +115,7 @@ constexpr int kPartialFloats = kBM * 256;  // one CTA's fp32 partial tile (up to
 struct UnitIter {
     int next_dp, stride;
     long long it, it_end;
+    int ndp;  // data-parallel units handed out so far
 };
 
 // First stream-K iteration of cluster c: the sk_tiles * k_blocks iterations
@@ -126,6 +127,7 @@ __device__ __forceinline__ long long sk_begin(const KernelParams& p, int c) {
 __device__ __forceinline__ void unit_iter_init(UnitIter& u, const KernelParams& p, int c, int clusters) {
     u.next_dp = c;
     u.stride = clusters;
+    u.ndp = 0;
     if (p.sk_tiles > 0 && c < p.sk_pairs) {
         u.it = sk_begin(p, c);
         u.it_end = sk_begin(p, c + 1);
@@ -153,6 +155,7 @@ __device__ __forceinline__ bool unit_next(UnitIter& u, const KernelParams& p, in
     if (u.next_dp < p.dp_tiles) {
         tile = u.next_dp;
         u.next_dp += u.stride;
+        ++u.ndp;
         k0 = 0;
         k1 = p.k_blocks;
         return true;

@@ -183,7 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (split > 1) k0 = kb_begin, k1 = kb_end;
                 int mb, nb;
                 tile_coords(t, p, mb, nb);
-                for (int kb = k0; kb < k1; ++kb) {
+                // every second data-parallel tile of a CTA walks K backwards: it
+                // starts on the K range the CTA's previous tile ended on, still in L2
+                const bool rev = split == 1 && k0 == 0 && k1 == p.k_blocks && (u.ndp & 1) == 0;
+                for (int kb0 = k0; kb0 < k1; ++kb0) {
+                    const int kb = rev ? k1 - 1 - (kb0 - k0) : kb0;
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;

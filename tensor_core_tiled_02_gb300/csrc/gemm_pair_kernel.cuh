@@ -160,7 +160,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_coords(t, p, mb, nb);
                 const int m0 = mb * PM + (int)rank * L::kRows;
                 const int n0 = nb * PN + (int)rank * (PN / 2);
-                for (int kb = k0; kb < k1; ++kb) {
+                // every second data-parallel tile walks K backwards: it starts on the
+                // K range the cluster's previous tile (same row block of A) ended on,
+                // still in L2
+                const bool rev = k0 == 0 && k1 == KB && (u.ndp & 1) == 0;
+                for (int kb0 = k0; kb0 < k1; ++kb0) {
+                    const int kb = rev ? k1 - 1 - (kb0 - k0) : kb0;
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
