@@ -90,6 +90,8 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 
 // Grouped raster: groups of `g` m-blocks; inside a group the m-block varies
 // fastest, so consecutive tile ids share B columns and a few A rows in L2.
+// Every second group walks the n-blocks backwards (a serpentine), so a group
+// starts on the columns of B the group before it ended on, still in L2.
 __device__ __forceinline__ void tile_coords(int t, const KernelParams& p, int& mb, int& nb) {
     const int g = p.raster_group;
     const int per_group = g * p.tiles_n;
@@ -99,6 +101,7 @@ __device__ __forceinline__ void tile_coords(int t, const KernelParams& p, int& m
     const int r = t - grp * per_group;
     mb = first_m + r % gm;
     nb = r / gm;
+    if (grp & 1) nb = p.tiles_n - 1 - nb;
 }
 
 __device__ __forceinline__ void record_timeout(unsigned site) { atomicCAS(&g_status, 0u, site); }
