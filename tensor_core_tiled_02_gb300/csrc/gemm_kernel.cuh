@@ -59,8 +59,9 @@
 // slot, expect-tx) run before `griddepcontrol.wait`, so they overlap the tail
 // of the previous kernel in the stream.  Each role waits just before its first
 // global-memory access: the producer before its first TMA load, the epilogue
-// on entering its role; the MMA warp touches only shared and tensor memory
-// and never waits.  The set-up is worth moving: the first pass through each
+// before its first access to C or the workspace (after its dry drain, when it
+// runs one); the MMA warp touches only shared and tensor memory and never
+// waits.  The set-up is worth moving: the first pass through each
 // code path misses the instruction cache, about 500 cycles a time, and on
 // the critical path after the wait those misses cost ~0.85 us per launch.
 //

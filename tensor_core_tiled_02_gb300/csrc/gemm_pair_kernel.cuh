@@ -29,7 +29,8 @@
 // Persistent: cluster c walks pair tiles c, c + clusters, ... in the grouped
 // raster.  Programmatic dependent launch as in the single-CTA kernel: the
 // producer waits for the previous kernel just before its first TMA load, the
-// epilogue on entering its role, the MMA warp never.
+// epilogue just before its first access to C or the workspace (after its dry
+// drain, when it runs one), the MMA warp never.
 //
 // Stream-K (sk_tiles > 0): the K iterations of the tiles beyond the full
 // waves are split evenly over the first sk_pairs clusters, which run their
