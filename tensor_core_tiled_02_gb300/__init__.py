@@ -174,6 +174,20 @@ def gemm_f16_device_status(reset: bool = True):
     return rc, site.value
 
 
+def _check_device(*tensors) -> None:
+    """Every tensor handed to the library must live on one CUDA device: the
+    kernels take raw device pointers, and a host or another GPU's pointer
+    there is a user error caught here, not in a kernel."""
+    dev = None
+    for t in tensors:
+        if not t.is_cuda:
+            raise ValueError("every tensor must be a CUDA tensor")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"tensors on different devices: {dev} and {t.device}")
+
+
 def _out_code(out_dtype) -> int:
     import torch
 
@@ -197,6 +211,7 @@ def add_matrices(x, y, out=None, stream=None):
         out = torch.empty_like(x)
     elif out.dtype != torch.float32 or out.shape != x.shape or not out.is_contiguous():
         raise ValueError("out must be a contiguous f32 tensor of x's shape")
+    _check_device(x, y, out)
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -224,6 +239,7 @@ def matmul_acc(a, b, c, stream=None):
         raise ValueError("c must be an fp16 or fp32 [M, N] tensor")
     if not (a.is_contiguous() and b.is_contiguous() and c.is_contiguous()):
         raise ValueError("a, b and c must be contiguous row-major")
+    _check_device(a, b, c)
     if stream is None:
         stream = torch.cuda.current_stream(a.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -265,6 +281,7 @@ def matmul(a, b, out_dtype=None, out=None, stream=None, workspace=None):
         out = torch.empty((M, N), dtype=tdt, device=a.device)
     elif out.dtype != tdt or tuple(out.shape) != (M, N) or not out.is_contiguous():
         raise ValueError("out must be a contiguous [M, N] tensor of out_dtype")
+    _check_device(a, b, out, *([workspace] if workspace is not None else []))
     if stream is None:
         stream = torch.cuda.current_stream(a.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -272,8 +289,6 @@ def matmul(a, b, out_dtype=None, out=None, stream=None, workspace=None):
         if workspace is None:
             rc = gemm_f16(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, code, handle)
         else:
-            if not workspace.is_cuda:
-                raise ValueError("workspace must be a CUDA tensor")
             rc = gemm_f16_ws(a.data_ptr(), b.data_ptr(), out.data_ptr(), M, N, K, code, workspace.data_ptr(),
                              workspace.numel() * workspace.element_size(), handle)
     if rc != 0:
