@@ -130,7 +130,10 @@ typedef struct {
  *              and C is valid once the stream reaches this point
  *
  * Pointers may be NULL only where nothing is read or written through them
- * (A and B when K == 0; all three when M == 0 or N == 0).
+ * (A and B when K == 0; all three when M == 0 or N == 0).  All three must
+ * point into memory of the current device: the call does not ask the driver
+ * where a pointer points, so host memory or another device's memory is not
+ * detected here (the Python binding checks its tensors).
  * Errors: GEMM_ERR_DTYPE, GEMM_ERR_DIM, GEMM_ERR_NULL, GEMM_ERR_ALIGN,
  * GEMM_ERR_ALIAS, GEMM_ERR_CONFIG before any CUDA call; GEMM_ERR_CUDA,
  * GEMM_ERR_ARCH, GEMM_ERR_TMAP, GEMM_ERR_LAUNCH after.  A device-side timeout
