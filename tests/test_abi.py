@@ -347,3 +347,63 @@ def test_plan_null_out(lib):
     assert lib.gemm_f16_plan(128, 128, 64, 0, 152, None) == NULL
     assert lib.gemm_f16_get_config(None) == NULL
 
+
+
+def _check_plan(p, M, N, K, auto):
+    """Invariants every plan must satisfy, whatever the shape or config."""
+    cdiv = lambda a, b: -(-a // b)
+    assert (p["tiles_m"], p["tiles_n"]) == (cdiv(M, p["tile_m"]), cdiv(N, p["tile_n"]))
+    assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
+    assert p["k_steps"] == cdiv(K, p["tile_k"])
+    assert p["stages"] > p["release"] >= 0 and p["slots"] == p["stages"] + p["release"]
+    assert p["smem_bytes"] <= 232448 and p["threads"] == 192
+    # one CTA per SM at most as far as TMEM goes: no CTA ever waits on another's columns
+    assert 233472 // (p["smem_bytes"] + 1024) * p["tmem_cols"] <= 512
+    if p["cta_group"] == 2:
+        assert p["split"] == 1 and p["grid"] % 2 == 0 and 2 <= p["grid"] <= 152
+        assert (p["tile_m"], p["tile_n"], p["tmem_cols"]) in ((256, 256, 512), (128, 128, 128))
+        if p["sk_tiles"] > 0:
+            # stream-K owners wait on other pairs: every pair resident at once
+            assert p["sk_pairs"] <= p["grid"] // 2 <= RESIDENT[2]
+            assert p["dp_tiles"] + p["sk_tiles"] == p["num_tiles"]
+            assert 0 < p["workspace_bytes"] <= 20 << 20  # gemm_f16_noalloc's array holds it
+        else:
+            assert p["dp_tiles"] == p["num_tiles"]
+    else:
+        assert p["tile_m"] == 128 and p["tile_n"] in (64, 128, 256) and p["tmem_cols"] == 2 * p["tile_n"]
+        if p["split"] > 1:
+            assert p["grid"] == p["num_tiles"] * p["split"] and p["split"] <= p["k_steps"]
+            if auto:
+                assert p["num_tiles"] <= RESIDENT[p["split"]]
+        elif p["sk_tiles"] > 0:
+            assert p["grid"] == p["sk_pairs"] <= 152 and p["dp_tiles"] == 0 and p["sk_tiles"] == p["num_tiles"]
+        else:
+            assert 1 <= p["grid"] <= 152 and p["dp_tiles"] == p["num_tiles"]
+
+
+def test_plan_invariants_on_random_shapes(lib):
+    """Seeded random shapes (ragged, K = 0 included) under the planner and
+    under forced configurations: every plan keeps the invariants above, and a
+    forced configuration either plans or is refused as GEMM_ERR_CONFIG."""
+    import numpy as np
+
+    rng = np.random.default_rng(20261202)
+    configs = [({}, True), (dict(cta_group=2), False), (dict(cta_group=2, tile_n=128), False),
+               (dict(cta_group=2, stream_k=2), False), (dict(cta_group=1, stream_k=2), False),
+               (dict(split=2), False), (dict(split=5, tile_n=64), False), (dict(tile_n=256, stages=2), False)]
+    try:
+        for i in range(1500):
+            M = int(rng.integers(1, 20000)) if i % 4 else int(rng.integers(1, 400))
+            N = 8 * int(rng.integers(1, 2500))
+            K = 8 * int(rng.integers(0, 5000)) if i % 3 else 8 * int(rng.integers(0, 64))
+            cfg, auto = configs[i % len(configs)]
+            tc.gemm_f16_set_config(**cfg)
+            for ws in (False, True):
+                try:
+                    p = tc.gemm_f16_plan(M, N, K, i % 2, num_sms=152, with_workspace=ws)
+                except tc.GemmError as e:
+                    assert not auto and e.code == CONFIG, (M, N, K, cfg)
+                    continue
+                _check_plan(p, M, N, K, auto)
+    finally:
+        tc.gemm_f16_set_config()
