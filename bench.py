@@ -16,6 +16,12 @@ Prints ONE JSON line (rank 0):
              launch time from CUDA events) against the measured dense peak
   cpu_baseline  the CPU oracle timed on a bounded sample of the same workload
   clocks     SM clocks and throttle reasons sampled during the timed region
+  configs    after the headline, every one of the five workloads (256^3,
+             4096^3, 8192^3, the M = 128 skinny product, long K with fp32 out)
+             timed on its own: inputs rotated past L2, at least 20 launches
+             back to back, eager and replayed from a CUDA graph; per config
+             the milliseconds per launch, TFLOP/s, GB/s, its roofline (the
+             tensor peak or the HBM copy rate, whichever binds) and its plan
 
 ``--impl reference`` times the CPU oracle instead (the reference arm): each
 step computes a bounded sample of rows of the same product on the host cores.
@@ -61,6 +67,9 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--configs", default="all",
+                    help="per-config leg after the headline: 'all', 'none' or a comma list of workloads")
+    ap.add_argument("--config-ms", type=float, default=30.0, help="timed milliseconds per config (at least 20 launches)")
     return ap.parse_args(argv)
 
 
@@ -354,6 +363,125 @@ def gemm_roofline(w, launch_s: float) -> dict:
     return hbm
 
 
+CONFIG_WORKLOADS = ["gemm_256", "gemm_4096", "gemm_8192", "skinny", "long_k"]
+PLAN_KEYS = ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "release", "slots", "split", "grid",
+             "raster_group", "num_tiles", "k_steps", "dp_tiles", "sk_tiles", "sk_pairs", "workspace_bytes")
+
+
+def rotation_copies(set_bytes: int, l2_bytes: int) -> int:
+    """Input sets to rotate over so that a launch's operands were last touched
+    at least twice the L2 capacity of other data ago (at least 3 sets)."""
+    return max(3, math.ceil(2 * l2_bytes / max(set_bytes, 1)))
+
+
+def kernel_name(w, plan) -> str:
+    if plan["cta_group"] == 2:
+        return f"gemm_f16_pair_kernel<{w.out_dtype},{plan['tile_k']},{plan['tile_m']},{plan['tile_n']}>"
+    return f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>"
+
+
+def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dict:
+    """Time the GEMM of one workload on the device.  Inputs and outputs are
+    rotated over enough copies that each launch reads operands evicted from
+    L2.  Two timings, each with CUDA events on the launching stream around at
+    least 20 back-to-back launches: `eager` (one ctypes call per launch, so
+    host overhead shows for launches of a few microseconds) and `graph` (the
+    same launches captured once in a CUDA graph and replayed: the kernels'
+    own time).  The roofline uses the graph figure."""
+    import torch
+
+    import tensor_core_tiled_02_gb300 as tc
+
+    out_t = torch.float16 if w.out_dtype == 0 else torch.float32
+    copies = rotation_copies(w.bytes_moved, l2_bytes)
+    A = torch.empty((copies, w.M, w.K), dtype=torch.float16, device=dev)
+    B = torch.empty((copies, w.K, w.N), dtype=torch.float16, device=dev)
+    C = torch.empty((copies, w.M, w.N), dtype=out_t, device=dev)
+    A.copy_(a_cpu.to(dev).unsqueeze(0).expand_as(A))
+    B.copy_(b_cpu.to(dev).unsqueeze(0).expand_as(B))
+    ws = tc.workspace(w.M, w.N, w.K, w.out_dtype, device=dev)
+    plan = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, with_workspace=ws is not None)
+    ws_ptr = ws.data_ptr() if ws is not None else 0
+    ws_bytes = ws.numel() if ws is not None else 0
+    ptrs = [(A[j].data_ptr(), B[j].data_ptr(), C[j].data_ptr()) for j in range(copies)]
+
+    def launch(i, handle):
+        a, b, c = ptrs[i % copies]
+        rc = tc.gemm_f16_ws(a, b, c, w.M, w.N, w.K, w.out_dtype, ws_ptr, ws_bytes, handle)
+        if rc != 0:
+            raise tc.GemmError(rc)
+
+    def timed(fn, stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / 1e3
+
+    cur = torch.cuda.current_stream(dev)
+    h = cur.cuda_stream
+    for i in range(5):
+        launch(i, h)
+    est = timed(lambda: [launch(i, h) for i in range(10)], cur) / 10
+    n = int(min(2000, max(20, math.ceil(target_s / max(est, 1e-7)))))
+    eager_s = timed(lambda: [launch(i, h) for i in range(n)], cur)
+
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(cur)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(n):
+            launch(i, side.cuda_stream)
+    cur.wait_stream(side)
+    g.replay()
+    reps = int(max(1, math.ceil(target_s / max(n * est, 1e-7))))
+    graph_s = timed(lambda: [g.replay() for _ in range(reps)], cur)
+    rc, site = tc.gemm_f16_device_status(reset=True)
+    if rc != 0:
+        raise RuntimeError(f"{w.name}: device wait gave up (site {site})")
+    launch_s = graph_s / (n * reps)
+    roof = gemm_roofline(w, launch_s)
+    roof["traffic"] = recorded_traffic(w.name, plan)
+    roof["kernel"] = kernel_name(w, plan)
+    entry = {"M": w.M, "N": w.N, "K": w.K, "out_dtype": "f16" if w.out_dtype == 0 else "f32",
+             "ms_per_launch": launch_s * 1e3, "eager_ms_per_launch": eager_s / n * 1e3,
+             "launches": n * reps + n, "tflops": w.flops / launch_s / 1e12,
+             "gbs": w.bytes_moved / launch_s / 1e9, "roofline": roof,
+             "inputs": f"A ~ {w.a_dist[0]}({w.a_dist[1]:g}), B ~ {w.b_dist[0]}({w.b_dist[1]:g}), fp16, seeds 0/1",
+             "l2": f"rotated over {copies} copies of A, B and C, {w.bytes_moved / 1e6:.1f} MB each, "
+                   f"{copies * w.bytes_moved / 1e6:.0f} MB in all (> 2x L2)",
+             "plan": {k: plan[k] for k in PLAN_KEYS}}
+    if roof["frac"] < 0.2:
+        entry["regime"] = ("launch latency: the roofline time is a small part of the launch, which is "
+                           "fixed prologue, pipeline fill and drain")
+    del A, B, C, ws, g
+    return entry
+
+
+def run_configs(args, dev, l2_bytes: int, cached_inputs: dict) -> dict:
+    """The per-config leg: every workload of the five, one after another."""
+    import torch
+
+    from tensor_core_tiled_02_gb300.synthetic import WORKLOADS, workload_inputs
+
+    names = CONFIG_WORKLOADS if args.configs == "all" else [n for n in args.configs.split(",") if n]
+    out = {}
+    clocks = ClockSampler(dev.index or 0, enabled=not args.no_clocks)
+    clocks.start()
+    for name in names:
+        w = WORKLOADS[name]
+        a_cpu, b_cpu = cached_inputs.get(name) or workload_inputs(w)
+        out[name] = time_one_config(w, dev, a_cpu, b_cpu, args.config_ms / 1e3, l2_bytes)
+        torch.cuda.empty_cache()
+    summary = clocks.stop()
+    if summary is not None:
+        out["clocks"] = summary
+    return out
+
+
 def workload_config(w, plan, copies: int | None = None) -> dict:
     cfg = {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
            "out_dtype": "f16" if w.out_dtype == 0 else "f32",
@@ -441,12 +569,17 @@ def run_ours(args, w, dist: Dist):
     if args.e2e_steps > 0:
         e2e = run_e2e(args, w, dist, dev, stream, a_cpu, b_cpu, out_t, ws)
 
+    configs = None
+    if args.configs != "none":
+        del As, Bs, Cs
+        torch.cuda.empty_cache()
+        l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2 ** 20)
+        configs = run_configs(args, dev, l2, {w.name: (a_cpu, b_cpu)})
+
     if dist.rank == 0:
         roofline = gemm_roofline(w, avg_launch_s)
         roofline["traffic"] = recorded_traffic(w.name, plan)
-        roofline["kernel"] = (f"gemm_f16_pair_kernel<{w.out_dtype},{plan['tile_k']},{plan['tile_m']},{plan['tile_n']}>"
-                              if plan["cta_group"] == 2
-                              else f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>")
+        roofline["kernel"] = kernel_name(w, plan)
         roofline["avg_launch_ms"] = avg_launch_s * 1e3
         cpu = None
         if not args.no_cpu_baseline and dist.world == 1:
@@ -465,6 +598,8 @@ def run_ours(args, w, dist: Dist):
             "gpu_launches": args.steps,
             "clocks": clock_summary,
         }
+        if configs is not None:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     dist.close()
     return 0

@@ -159,15 +159,22 @@ int gemm_f16_acc(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N
  * As gemm_f16, with a caller-owned device workspace for stream-K.  When the
  * tiles of the CTA-pair kernel do not fill the last wave, the K iterations of
  * that wave's tiles are shared evenly by the pairs, whose partial tiles meet
- * through the workspace (flags and fp32 partials).  `workspace_bytes` must be
- * at least what gemm_f16_workspace_size reports, else GEMM_ERR_WORKSPACE.
+ * through the workspace.  `workspace_bytes` must be at least what
+ * gemm_f16_workspace_size reports, else GEMM_ERR_WORKSPACE.
  *
  *   workspace  device pointer, 256-byte aligned; zero-filled by the caller
  *              before its FIRST use with this library (the library keeps it
  *              valid for later calls); NULL runs exactly as gemm_f16
+ *   layout     16 KiB of flags (one 32-bit word per epilogue warp of up to
+ *              1024 CTAs), then one 128 x 256 fp32 partial tile (128 KiB) per
+ *              CTA that shares tiles.  A flag holds 0 or the value of the
+ *              launch whose partial is ready; the warp that consumes a
+ *              partial sets its flag back to 0, so a launch captured in a
+ *              CUDA graph and replayed waits for each replay's own partials.
  *   ownership  the caller's; it may be reused by the next call on the same
  *              stream, but two calls that may overlap on the GPU must not
- *              share one workspace
+ *              share one workspace.  After a launch that reported
+ *              GEMM_ERR_DEVICE_TIMEOUT, zero it again before reuse.
  * Errors: those of gemm_f16, GEMM_ERR_ALIGN for a misaligned workspace and
  * GEMM_ERR_WORKSPACE for a short one.
  */
@@ -183,15 +190,18 @@ int gemm_f16_ws(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, int N,
  * The pages have no counterpart; this is an interface convenience of this
  * library.
  *
- * The stream-K scratch lives in one fixed array of 20 MiB in device memory,
- * which every GPU that loads this library holds until the process exits.
- * Nothing is allocated or freed by the call.  A problem whose plan needs more
- * scratch than that (more than about 80 CTA pairs sharing tiles) is refused
- * with GEMM_ERR_SCRATCH_LIMIT.
+ * The stream-K scratch lives in one fixed array of 20 MiB + 16 KiB in device
+ * memory (the 16 KiB of flags and the 128 KiB partial tiles of at most 160
+ * CTAs, i.e. 80 CTA pairs), which every GPU that loads this library holds
+ * until the process exits.  Nothing is allocated or freed by the call.  A
+ * problem whose plan shares tiles over more than 160 CTAs (possible only on a
+ * part with more than 160 SMs) is refused with GEMM_ERR_SCRATCH_LIMIT.
  *
  *   - The first call on each device looks up the array's device address (a
- *     runtime query, no allocation).  Make that first call before any stream
- *     capture on that device.
+ *     runtime query, no allocation) and keeps it for later calls.  Make that
+ *     first call before any stream capture on that device.  A device reset
+ *     (cudaDeviceReset) makes the kept address stale: do not call this entry
+ *     point on that device again in the same process.
  *   - All calls share the one array and it keeps what the last call wrote.
  *     Two calls whose kernels may overlap on the GPU (different streams, or
  *     different host threads, without ordering between them) race on it and
@@ -208,9 +218,15 @@ int gemm_f16_noalloc(const gemm_f16_t *A, const gemm_f16_t *B, void *C, int M, i
 int gemm_f16_workspace_size(int M, int N, int K, int out_dtype, int num_sms, size_t *bytes);
 
 /*
- * The plan gemm_f16 would use for this problem under the current config.
- * num_sms > 0 plans for that many SMs without touching CUDA (host-only);
- * num_sms == 0 asks the current device.  `out` is caller-owned host memory.
+ * The plan gemm_f16 would use for this problem under the current config: the
+ * tiling, the grid of output tiles and the sequential K pipeline of "Quickstart:
+ * GPU" ("Pipelining: a matmul kernel": grid (m // tile_m, n // tile_n), K /
+ * tile_k steps), and the max_concurrent_steps / delay_release pair with the
+ * validation and clamping of "JAX Pallas Mosaic GPU 快速上手" ("深入emit_pipeline
+ * 的关键参数").  Ragged shapes are planned, not refused: the tile counts are
+ * ceilings.  num_sms > 0 plans for that many SMs without touching CUDA
+ * (host-only, for tests and tools); num_sms == 0 asks the current device.
+ * `out` is caller-owned host memory.
  * Errors: as gemm_f16's argument checks (pointers excepted), GEMM_ERR_NULL
  * for out == NULL, GEMM_ERR_CUDA when num_sms == 0 and no device answers.
  */
@@ -220,6 +236,10 @@ int gemm_f16_plan(int M, int N, int K, int out_dtype, int num_sms, gemm_plan *ou
 int gemm_f16_plan_ws(int M, int N, int K, int out_dtype, int num_sms, gemm_plan *out);
 
 /* Replace the process-wide tuning config (copied); NULL restores defaults.
+ * Its stages and release fields are emit_pipeline's max_concurrent_steps and
+ * delay_release ("JAX Pallas Mosaic GPU 快速上手", "深入emit_pipeline的关键参数"),
+ * tile_n and tile_k the tile of "Quickstart: GPU" ("Pipelining: a matmul
+ * kernel"); as there, stages must exceed release.
  * A call running at the same time on another host thread plans with either
  * the old or the new config, never a mix.
  * Errors: GEMM_ERR_CONFIG for an out-of-range field (the old config stays). */
@@ -228,7 +248,8 @@ int gemm_f16_set_config(const gemm_config *cfg);
 /* Copy the current tuning config into caller-owned `out`. */
 int gemm_f16_get_config(gemm_config *out);
 
-/* Static, NUL-terminated description of a gemm_status code. */
+/* Static, NUL-terminated description of a gemm_status code.  No counterpart
+ * on the pages (Pallas raises Python exceptions instead). */
 const char *gemm_f16_strerror(int code);
 
 /*

@@ -151,11 +151,14 @@ int max_slots_for_pair(int out_dtype, int step_k, int pair_m) {
 }
 
 // Workspace of a stream-K plan shared by `ctas` CTAs: a flag per epilogue
-// warp of every CTA (rounded up to 256 bytes), then one fp32 partial of up to
-// 128 x 256 per CTA.
-size_t flag_bytes_for(int ctas) { return ((size_t)ctas * 4 * sizeof(unsigned) + 255) / 256 * 256; }
+// warp of up to kMaxSkCtas CTAs, then one fp32 partial of up to 128 x 256 per
+// CTA.  The flag area has the same size in every plan, so a flag word never
+// lies where another plan keeps a partial tile: it only ever holds 0 or the
+// epoch of some launch.
+constexpr int kMaxSkCtas = 1024;
+constexpr size_t kFlagBytes = (size_t)kMaxSkCtas * 4 * sizeof(unsigned);  // 16 KiB
 
-size_t workspace_for(int ctas) { return flag_bytes_for(ctas) + (size_t)ctas * kPartialFloats * sizeof(float); }
+constexpr size_t workspace_for(int ctas) { return kFlagBytes + (size_t)ctas * kPartialFloats * sizeof(float); }
 
 // Clusters the GPU can hold at once, by cluster size (one CTA per SM): [1] the
 // SMs, [2] CTA pairs, [3 .. kMaxSplit] split-K clusters.  Not every size packs
@@ -291,7 +294,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, b
         p->dp_tiles = p->num_tiles;
         int sk_tiles = 0, sk_pairs = 0, clusters = pairs;
         if (cfg.stream_k == 2) {
-            clusters = max_pairs;
+            clusters = max_pairs < kMaxSkCtas / 2 ? max_pairs : kMaxSkCtas / 2;
             sk_tiles = p->num_tiles;
             const long long iters = (long long)sk_tiles * p->k_steps;
             sk_pairs = (int)(iters < clusters ? iters : clusters);
@@ -301,7 +304,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, b
                 int parts = max_pairs / R;
                 if (parts > 4) parts = 4;
                 if (parts > p->k_steps / 8) parts = p->k_steps / 8;
-                if (parts >= 2) {
+                if (parts >= 2 && 2 * parts * R <= kMaxSkCtas) {
                     sk_tiles = R;
                     sk_pairs = parts * R;
                     clusters = p->num_tiles < max_pairs ? sk_pairs : pairs;
@@ -349,6 +352,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, b
         const long long iters = (long long)p->num_tiles * p->k_steps;
         long long ctas = iters / 16;
         if (ctas > num_sms) ctas = num_sms;
+        if (ctas > kMaxSkCtas) ctas = kMaxSkCtas;
         if (ctas < 1) ctas = 1;
         p->workspace_bytes = (long long)workspace_for((int)ctas);
         if (with_workspace) {
@@ -600,22 +604,13 @@ gemm_config current_config() {
     return g_cfg;
 }
 
-int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype, void* workspace,
-        size_t workspace_bytes, gemm_stream_t stream, bool accumulate = false) {
-    int rc = check_args(A, B, C, M, N, K, out_dtype, true);
-    if (rc == 1) return GEMM_OK;
-    if (rc != GEMM_OK) return rc;
-    if (workspace && ((uintptr_t)workspace & 255)) return GEMM_ERR_ALIGN;
-    const gemm_config cfg = current_config();
-    DeviceInfo* dev = nullptr;
-    rc = device_info(&dev);
-    if (rc != GEMM_OK) return rc;
-    if (dev->cc != 103) return GEMM_ERR_ARCH;
-    gemm_plan plan;
-    rc = plan_impl(M, N, K, out_dtype, dev->sms, fit_of(*dev), workspace != nullptr, cfg, &plan);
-    if (rc != GEMM_OK) return rc;
-    if (plan.sk_tiles > 0 && (size_t)plan.workspace_bytes > workspace_bytes) return GEMM_ERR_WORKSPACE;
-
+// Encode the tensor maps and launch one planned problem (arguments already
+// checked; `plan` made with `cfg` for this device; the workspace, if the plan
+// uses one, large enough).
+int launch_planned(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype,
+                   void* workspace, gemm_stream_t stream, bool accumulate, const gemm_config& cfg,
+                   const gemm_plan& plan, DeviceInfo* dev) {
+    int rc = GEMM_OK;
     std::call_once(g_encode_once, init_encode);
     if (!g_encode) return GEMM_ERR_CUDA;
     CUtensorMap ta, tb, tc;
@@ -659,8 +654,7 @@ int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, 
         if (e == 0) e = ++g_epoch;  // 0 is what a fresh (zero-filled) workspace holds
         kp.epoch = e;
         kp.flags = reinterpret_cast<unsigned*>(workspace);
-        kp.ws = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) +
-                                         flag_bytes_for(plan.sk_pairs * plan.cta_group));
+        kp.ws = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + kFlagBytes);
     }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -681,6 +675,24 @@ int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, 
                                          : launch<64, 1>(plan, ta, tb, tc, kp, s, *dev);
     return out_dtype == GEMM_OUT_F16 ? launch<128, 0>(plan, ta, tb, tc, kp, s, *dev)
                                      : launch<128, 1>(plan, ta, tb, tc, kp, s, *dev);
+}
+
+int run(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int N, int K, int out_dtype, void* workspace,
+        size_t workspace_bytes, gemm_stream_t stream, bool accumulate = false) {
+    int rc = check_args(A, B, C, M, N, K, out_dtype, true);
+    if (rc == 1) return GEMM_OK;
+    if (rc != GEMM_OK) return rc;
+    if (workspace && ((uintptr_t)workspace & 255)) return GEMM_ERR_ALIGN;
+    const gemm_config cfg = current_config();
+    DeviceInfo* dev = nullptr;
+    rc = device_info(&dev);
+    if (rc != GEMM_OK) return rc;
+    if (dev->cc != 103) return GEMM_ERR_ARCH;
+    gemm_plan plan;
+    rc = plan_impl(M, N, K, out_dtype, dev->sms, fit_of(*dev), workspace != nullptr, cfg, &plan);
+    if (rc != GEMM_OK) return rc;
+    if (plan.sk_tiles > 0 && (size_t)plan.workspace_bytes > workspace_bytes) return GEMM_ERR_WORKSPACE;
+    return launch_planned(A, B, C, M, N, K, out_dtype, workspace, stream, accumulate, cfg, plan, dev);
 }
 
 int plan_entry(int M, int N, int K, int out_dtype, int num_sms, bool with_workspace, gemm_plan* out) {
@@ -767,7 +779,7 @@ const char* gemm_f16_strerror(int code) {
         case GEMM_ERR_DEVICE_TIMEOUT: return "a kernel's bounded device-side wait ran out";
         case GEMM_ERR_WORKSPACE: return "the workspace is smaller than gemm_f16_workspace_size reports";
         case GEMM_ERR_SCRATCH_LIMIT:
-            return "the problem needs more stream-K scratch than gemm_f16_noalloc's fixed 20 MiB array holds";
+            return "the problem needs more stream-K scratch than gemm_f16_noalloc's fixed array holds (160 CTAs' partial tiles)";
         default: return "unknown gemm_status code";
     }
 }
@@ -871,11 +883,16 @@ int add_matrices_f32(const float* X, const float* Y, float* Z, int M, int N, gem
 
 namespace {
 
-// The scratch: kNoAllocScratchBytes of device memory in every GPU that loads
-// this library, held until the process exits.  Zero at module load.  Calls
-// share it and it keeps what the last call wrote; the flags only ever hold the
-// launch epoch of an earlier call, which never matches a later call's.
-constexpr size_t kNoAllocScratchBytes = 20u << 20;  // 20 MiB: 76 CTA pairs' partials need 19.0 MiB
+// The scratch: room for the flags and the partial tiles of kNoAllocMaxCtas
+// CTAs (80 CTA pairs, more than a 152-SM GB300 ever shares), held in every
+// GPU that loads this library until the process exits.  Zero at module load.
+// Calls share it and it keeps what the last call wrote.  A flag word only
+// ever holds 0 or some launch's epoch (the flag area has one fixed size, so
+// no plan keeps a partial tile there), and an epoch never repeats from one
+// launch to the next; an owner zeroes each flag it has consumed.
+constexpr int kNoAllocMaxCtas = 160;
+constexpr size_t kNoAllocScratchBytes = workspace_for(kNoAllocMaxCtas);  // 20 MiB + 16 KiB
+static_assert(kNoAllocScratchBytes == (20u << 20) + kFlagBytes, "scratch size as documented");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mu;
@@ -910,16 +927,21 @@ extern "C" int gemm_f16_noalloc(const gemm_f16_t* A, const gemm_f16_t* B, void* 
     int rc = check_args(A, B, C, M, N, K, out_dtype, true);
     if (rc == 1) return GEMM_OK;
     if (rc != GEMM_OK) return rc;
+    // one read of the config and one plan serve both the size check and the launch
+    const gemm_config cfg = current_config();
     DeviceInfo* dev = nullptr;
     rc = device_info(&dev);
     if (rc != GEMM_OK) return rc;
     if (dev->cc != 103) return GEMM_ERR_ARCH;
     gemm_plan plan;
-    rc = plan_impl(M, N, K, out_dtype, dev->sms, fit_of(*dev), true, current_config(), &plan);
+    rc = plan_impl(M, N, K, out_dtype, dev->sms, fit_of(*dev), true, cfg, &plan);
     if (rc != GEMM_OK) return rc;
     if (plan.sk_tiles > 0 && (size_t)plan.workspace_bytes > kNoAllocScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
+    // looked up on every call (cached after the first on this device), whether
+    // or not this plan shares tiles, so the first call does the set-up
     void* scratch = nullptr;
     rc = noalloc_scratch(&scratch);
     if (rc != GEMM_OK) return rc;
-    return run(A, B, C, M, N, K, out_dtype, scratch, kNoAllocScratchBytes, stream);
+    return launch_planned(A, B, C, M, N, K, out_dtype, plan.sk_tiles > 0 ? scratch : nullptr, stream, false, cfg,
+                          plan, dev);
 }

@@ -455,6 +455,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         failed = true;
                         break;
                     }
+                    // every lane has acquired them: hand the flags back (zero), so a later
+                    // launch with the same epoch (a replayed CUDA graph) waits afresh
+                    __syncwarp();
+                    if (lane == 0)
+                        for (int qq = cl + 1; qq < q_end; ++qq) ptx::st_relaxed_gpu(p.flags + qq * 4 + q, 0u);
                 }
 
 #pragma unroll 1

@@ -309,6 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok) (void)ptx::ld_acquire_gpu(f);  // orders this lane's reads after the flag
                 }
                 if (!ok) break;
+                // every lane has acquired them: hand the flags back (zero), so a later
+                // launch with the same epoch (a replayed CUDA graph) waits afresh
+                __syncwarp();
+                if (lane == 0)
+                    for (int qq = cluster + 1; qq < q_end; ++qq) ptx::st_relaxed_gpu(p.flags + (qq * 2 + (int)rank) * 4 + q, 0u);
                 // the owner unit is its cluster's last, so the other accumulator is
                 // free: sum the contributors' partials into it while the MMAs run
                 UnitIter peek = u;

@@ -118,3 +118,17 @@ def test_gemm_roofline_picks_the_binding_peak(monkeypatch):
     nbytes = 2 * 128 * 8192 + 2 * 8192 * 8192 + 2 * 128 * 8192
     assert abs(sk["achieved"] - nbytes / 30e-6 / 1e9) < 1e-6
     assert abs(sk["frac"] - sk["achieved"] / 6700.0) < 1e-12 and 0 < sk["tensor_frac"] < sk["frac"]
+
+
+def test_config_leg_covers_the_five_workloads_past_l2():
+    from tensor_core_tiled_02_gb300.synthetic import WORKLOADS
+
+    assert bench.parse_args([]).configs == "all"
+    assert sorted(bench.CONFIG_WORKLOADS) == sorted(n for n, w in WORKLOADS.items() if w.kind == "gemm")
+    l2 = 129 * 2 ** 20
+    for name in bench.CONFIG_WORKLOADS:
+        w = WORKLOADS[name]
+        n = bench.rotation_copies(w.bytes_moved, l2)
+        # each launch's operands were last touched at least two L2s of other data ago
+        assert n >= 3 and (n - 1) * w.bytes_moved >= 2 * l2 - w.bytes_moved
+    assert bench.rotation_copies(393216, l2) == 688  # 256^3: 0.39 MB a set

@@ -534,3 +534,39 @@ def test_graph_capture_and_replay():
     torch.cuda.synchronize()
     assert torch.equal(c1.view(torch.int16), e1.view(torch.int16))
     assert torch.equal(c2.view(torch.int16), e2.view(torch.int16))
+
+
+def test_graph_replay_of_stream_k_waits_for_each_replays_partials():
+    """One stream-K launch (the thin last wave of 4096^3 shared through the
+    workspace) captured once and replayed with new operands in the same
+    buffers: every replay carries the same flag value, so each owner must
+    hand its consumed flags back (zero) for the next replay to wait on its
+    own partials.  Each replay equals an eager call on the same operands."""
+    M = N = K = 4096
+    plan = tc.gemm_f16_plan(M, N, K, 0, with_workspace=True)
+    assert plan["sk_tiles"] > 0
+    ws = tc.workspace(M, N, K, 0)
+    a_d = torch.empty((M, K), dtype=torch.float16, device="cuda")
+    b_d = torch.empty((K, N), dtype=torch.float16, device="cuda")
+    c = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    a1, b1 = make_inputs(M, N, K, ("uniform", 1.0), ("uniform", 1.0), seed_a=71, seed_b=72)
+    a_d.copy_(a1)
+    b_d.copy_(b1)
+    tc.matmul(a_d, b_d, out=c, workspace=ws)  # one-time set-up outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tc.matmul(a_d, b_d, out=c, workspace=ws)
+    for seed in (81, 82, 83):
+        a, b = make_inputs(M, N, K, ("uniform", 1.0), ("uniform", 1.0), seed_a=seed, seed_b=seed + 1)
+        a_d.copy_(a)
+        b_d.copy_(b)
+        c.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        got = c.clone()
+        want = tc.matmul(a_d, b_d, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"replay with seed {seed}"
