@@ -21,7 +21,9 @@ Prints ONE JSON line (rank 0):
              timed on its own: inputs rotated past L2, at least 20 launches
              back to back, eager and replayed from a CUDA graph; per config
              the milliseconds per launch, TFLOP/s, GB/s, its roofline (the
-             tensor peak or the HBM copy rate, whichever binds) and its plan
+             tensor peak or the HBM copy rate, whichever binds) and its plan;
+             then gemm_8192_sustained: the headline workload back to back for
+             a few seconds, at the power cap, with its clocks
 
 ``--impl reference`` times the CPU oracle instead (the reference arm): each
 step computes a bounded sample of rows of the same product on the host cores.
@@ -70,6 +72,8 @@ def parse_args(argv=None):
     ap.add_argument("--configs", default="all",
                     help="per-config leg after the headline: 'all', 'none' or a comma list of workloads")
     ap.add_argument("--config-ms", type=float, default=30.0, help="timed milliseconds per config (at least 20 launches)")
+    ap.add_argument("--sustained-s", type=float, default=3.0,
+                    help="seconds of back-to-back 8192^3 launches at the power cap (0 skips)")
     return ap.parse_args(argv)
 
 
@@ -387,7 +391,8 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dic
     least 20 back-to-back launches: `eager` (one ctypes call per launch, so
     host overhead shows for launches of a few microseconds) and `graph` (the
     same launches captured once in a CUDA graph and replayed: the kernels'
-    own time).  The roofline uses the graph figure."""
+    own time).  `ms_per_launch`, and the roofline, take the shorter of the
+    two."""
     import torch
 
     import tensor_core_tiled_02_gb300 as tc
@@ -427,6 +432,9 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dic
         launch(i, h)
     est = timed(lambda: [launch(i, h) for i in range(10)], cur) / 10
     n = int(min(2000, max(20, math.ceil(target_s / max(est, 1e-7)))))
+    # each timed leg starts after a short idle spell, so that both begin in the
+    # same power state (a leg started right after another runs nearer the cap)
+    time.sleep(0.2)
     eager_s = timed(lambda: [launch(i, h) for i in range(n)], cur)
 
     side = torch.cuda.Stream(dev)
@@ -438,16 +446,20 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dic
     cur.wait_stream(side)
     g.replay()
     reps = int(max(1, math.ceil(target_s / max(n * est, 1e-7))))
+    time.sleep(0.2)
     graph_s = timed(lambda: [g.replay() for _ in range(reps)], cur)
     rc, site = tc.gemm_f16_device_status(reset=True)
     if rc != 0:
         raise RuntimeError(f"{w.name}: device wait gave up (site {site})")
-    launch_s = graph_s / (n * reps)
+    # the kernel's duration: the graph replay when it is shorter (it carries
+    # no host launch cost), else the eager launches
+    launch_s = min(graph_s / (n * reps), eager_s / n)
     roof = gemm_roofline(w, launch_s)
     roof["traffic"] = recorded_traffic(w.name, plan)
     roof["kernel"] = kernel_name(w, plan)
     entry = {"M": w.M, "N": w.N, "K": w.K, "out_dtype": "f16" if w.out_dtype == 0 else "f32",
              "ms_per_launch": launch_s * 1e3, "eager_ms_per_launch": eager_s / n * 1e3,
+             "graph_ms_per_launch": graph_s / (n * reps) * 1e3,
              "launches": n * reps + n, "tflops": w.flops / launch_s / 1e12,
              "gbs": w.bytes_moved / launch_s / 1e9, "roofline": roof,
              "inputs": f"A ~ {w.a_dist[0]}({w.a_dist[1]:g}), B ~ {w.b_dist[0]}({w.b_dist[1]:g}), fp16, seeds 0/1",
@@ -459,6 +471,64 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dic
                            "fixed prologue, pipeline fill and drain")
     del A, B, C, ws, g
     return entry
+
+
+def time_sustained(w, dev, a_cpu, b_cpu, seconds: float, l2_bytes: int, sample_clocks: bool) -> dict:
+    """The headline workload back to back for `seconds` (eager launches,
+    inputs rotated past L2), long enough for the GPU to settle at its power
+    cap; clocks sampled during the run.  Its fraction is against both the
+    burst and the sustained measured peak."""
+    import torch
+
+    import tensor_core_tiled_02_gb300 as tc
+
+    out_t = torch.float16 if w.out_dtype == 0 else torch.float32
+    copies = rotation_copies(w.bytes_moved, l2_bytes)
+    As = [a_cpu.to(dev) for _ in range(copies)]
+    Bs = [b_cpu.to(dev) for _ in range(copies)]
+    Cs = [torch.empty((w.M, w.N), dtype=out_t, device=dev) for _ in range(copies)]
+    ws = tc.workspace(w.M, w.N, w.K, w.out_dtype, device=dev)
+    ws_ptr = ws.data_ptr() if ws is not None else 0
+    ws_bytes = ws.numel() if ws is not None else 0
+    cur = torch.cuda.current_stream(dev)
+
+    def launch(i):
+        j = i % copies
+        rc = tc.gemm_f16_ws(As[j].data_ptr(), Bs[j].data_ptr(), Cs[j].data_ptr(), w.M, w.N, w.K, w.out_dtype,
+                            ws_ptr, ws_bytes, cur.cuda_stream)
+        if rc != 0:
+            raise tc.GemmError(rc)
+
+    for i in range(3):
+        launch(i)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(5):
+        launch(i)
+    torch.cuda.synchronize(dev)
+    est = (time.perf_counter() - t0) / 5
+    n = max(20, int(seconds / max(est, 1e-6)))
+    clocks = ClockSampler(dev.index or 0, enabled=sample_clocks)
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for i in range(n):
+        launch(i)
+    e1.record(cur)
+    torch.cuda.synchronize(dev)
+    summary = clocks.stop()
+    rc, site = tc.gemm_f16_device_status(reset=True)
+    if rc != 0:
+        raise RuntimeError(f"sustained {w.name}: device wait gave up (site {site})")
+    launch_s = e0.elapsed_time(e1) / 1e3 / n
+    peaks, src = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tflops = w.flops / launch_s / 1e12
+    return {"workload": w.name, "seconds": launch_s * n, "launches": n, "ms_per_launch": launch_s * 1e3,
+            "tflops": tflops, "frac_of_burst": tflops / burst, "frac_of_sustained": tflops / sus,
+            "peak_source": f"bf16_tflops and bf16_tflops_sustained of {src}", "clocks": summary}
 
 
 def run_configs(args, dev, l2_bytes: int, cached_inputs: dict) -> dict:
@@ -479,6 +549,13 @@ def run_configs(args, dev, l2_bytes: int, cached_inputs: dict) -> dict:
     summary = clocks.stop()
     if summary is not None:
         out["clocks"] = summary
+    if args.sustained_s > 0:
+        w = WORKLOADS["gemm_8192"]
+        a_cpu, b_cpu = cached_inputs.get(w.name) or workload_inputs(w)
+        time.sleep(0.5)
+        out["gemm_8192_sustained"] = time_sustained(w, dev, a_cpu, b_cpu, args.sustained_s, l2_bytes,
+                                                    not args.no_clocks)
+        torch.cuda.empty_cache()
     return out
 
 
