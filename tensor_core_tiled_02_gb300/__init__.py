@@ -18,7 +18,10 @@ import os
 import threading
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libtcgemm.so")
+# TCGEMM_VARIANT=trace or =check selects a debug build of the same library
+# (libtcgemm_trace.so, libtcgemm_check.so; see build.py); unset: the product
+_VARIANT = os.environ.get("TCGEMM_VARIANT", "")
+LIB_PATH = os.path.join(_HERE, f"libtcgemm_{_VARIANT}.so" if _VARIANT else "libtcgemm.so")
 
 GEMM_OUT_F16 = 0
 GEMM_OUT_F32 = 1

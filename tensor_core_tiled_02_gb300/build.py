@@ -20,6 +20,20 @@ LIB = os.path.join(PKG, "libtcgemm.so")
 SOURCES = [os.path.join(CSRC, "gemm_f16.cu")]
 GENCODE = "arch=compute_103a,code=sm_103a"
 
+# Debug variants of the same sources, each its own library beside the product:
+#   trace  -DTCGEMM_TRACE: the kernels stamp %globaltimer and the SM clock per
+#          role, tile and K step into a buffer the caller hands the library
+#          (gemm_f16_trace_buffer, include/gemm_f16_trace.h); read by trace.py
+#   check  -DTCGEMM_CHECK: every shared-memory ring, staging and barrier
+#          address and every Tensor Memory column range is checked against
+#          its allocation before use; a violation skips the access and is
+#          reported through gemm_f16_device_status (sites 9 and 10)
+VARIANTS = {"trace": ["-DTCGEMM_TRACE"], "check": ["-DTCGEMM_CHECK"]}
+
+
+def variant_lib(name: str) -> str:
+    return LIB if not name else os.path.join(PKG, f"libtcgemm_{name}.so")
+
 
 def nvcc_path() -> str:
     for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
@@ -28,10 +42,13 @@ def nvcc_path() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def build(verbose_ptxas: bool = False, out: str = LIB, extra=()) -> str:
+def build(verbose_ptxas: bool = False, out: str | None = None, extra=(), variant: str = "") -> str:
+    if variant and variant not in VARIANTS:
+        raise ValueError(f"unknown variant {variant!r}")
+    out = out or variant_lib(variant)
     cmd = [nvcc_path(), "-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17",
            "-Xcompiler", "-fPIC", "-shared", "-I", INCLUDE, "-I", CSRC,
-           "-o", out, *SOURCES, *extra]
+           *(VARIANTS[variant] if variant else []), "-o", out, *SOURCES, *extra]
     if verbose_ptxas:
         cmd[1:1] = ["-Xptxas", "-v"]
     subprocess.run(cmd, check=True)
@@ -48,5 +65,5 @@ def needs_build() -> bool:
 
 
 if __name__ == "__main__":
-    build(verbose_ptxas="-v" in sys.argv)
-    print(LIB)
+    v = next((a for a in sys.argv[1:] if a in VARIANTS), "")
+    print(build(verbose_ptxas="-v" in sys.argv, variant=v))

@@ -7,6 +7,7 @@
 #include <cuda_fp16.h>
 #include <cstdint>
 
+#include "bounds.cuh"
 #include "ptx.cuh"
 
 namespace tcgemm {
@@ -30,6 +31,11 @@ enum WaitSite : unsigned {
     kSiteReduceReady = 6,
     kSiteReduceData = 7,
     kSitePartialFlag = 8,
+    // bounds-check build (TCGEMM_CHECK) only: an access outside its allocation
+    // was about to be made, and was skipped
+    kSiteSmemBounds = 9,       // shared memory: ring, staging, mbarrier, or the carve-up itself
+    kSiteTmemBounds = 10,      // Tensor Memory columns beyond the CTA's allocation
+    kSiteWorkspaceBounds = 11, // a stream-K workspace slot or flag beyond the plan's
 };
 
 __device__ unsigned int g_status;
@@ -52,6 +58,61 @@ struct KernelParams {
     float* ws;             // one 128 x 256 fp32 partial per CTA of the sharing clusters
     unsigned* flags;       // one flag per epilogue warp of those CTAs
     const void* c_in;      // accumulate into C: the values C holds before the call; NULL otherwise
+    // trace build only (TCGEMM_TRACE): this launch's records, NULL when not traced;
+    // trace_ctas CTAs x kTraceRoles roles x trace_events records of two words
+    unsigned long long* trace;
+    int trace_ctas, trace_events;
+};
+
+// ---- the trace build ------------------------------------------------------------
+// With -DTCGEMM_TRACE, lane 0 of each role records events of its own: the
+// producer (role 0), the MMA issuer (role 1) and the four epilogue warps (roles
+// 2..5).  A record is two 64-bit words: the SM clock (clock64), then the event
+// code (bits 63..56), its argument (bits 55..32) and, for the entry and exit
+// events only, the low 32 bits of %globaltimer in nanoseconds (the one clock
+// shared by all SMs, read only there: it is slow to read and ticks coarsely;
+// a reader places the other events between the two by the SM clock).
+// Without the define a Tracer is empty and every call vanishes.
+constexpr int kTraceRoles = 6;
+enum TraceEvent : unsigned {
+    kTrEntry = 1,       // kernel entry (arg: SM id)
+    kTrSetup = 2,       // barriers, TMEM and the cluster synchronised
+    kTrDepWait = 3,     // griddepcontrol.wait returned: the previous kernel is complete
+    kTrLoad = 4,        // producer issued a step's loads (arg: K step)
+    kTrFull = 5,        // MMA issuer saw a step's operands land (arg: K step)
+    kTrTileDone = 6,    // MMA issuer committed a unit's accumulator (arg: tile)
+    kTrAccReady = 7,    // epilogue saw the accumulator complete (arg: tile)
+    kTrPushed = 8,      // split-K: this warp's partials pushed to / parked for the other ranks
+    kTrPartner = 9,     // split-K: the other ranks' partials of this warp's chunks are here
+    kTrFlags = 10,      // stream-K owner: every contributor's flag seen
+    kTrStored = 11,     // a chunk's TMA store issued (arg: chunk)
+    kTrStoreRead = 12,  // the warp's stores have read their staging
+    kTrExit = 13,       // the role is about to leave the kernel
+    kTrParked = 14,     // stream-K contributor: partial parked and flag released
+};
+
+struct Tracer {
+#ifdef TCGEMM_TRACE
+    unsigned long long* rec = nullptr;
+    int n = 0, cap = 0;
+    __device__ __forceinline__ Tracer(const KernelParams& p, int role) {
+        if (p.trace != nullptr && (int)blockIdx.x < p.trace_ctas) {
+            rec = p.trace + 2ull * ((unsigned long long)(blockIdx.x * kTraceRoles + role) * p.trace_events);
+            cap = p.trace_events;
+        }
+    }
+    __device__ __forceinline__ void operator()(unsigned code, unsigned arg = 0) {
+        if (rec == nullptr || n >= cap) return;
+        const unsigned long long clk = clock64();
+        const unsigned gt = (code == kTrEntry || code == kTrExit) ? (unsigned)ptx::globaltimer() : 0u;
+        rec[2 * n] = clk;
+        rec[2 * n + 1] = ((unsigned long long)code << 56) | ((unsigned long long)(arg & 0xFFFFFFu) << 32) | gt;
+        ++n;
+    }
+#else
+    __device__ __forceinline__ Tracer(const KernelParams&, int) {}
+    __device__ __forceinline__ void operator()(unsigned, unsigned = 0) {}
+#endif
 };
 
 template <int BN, int OUT>
@@ -106,7 +167,24 @@ __device__ __forceinline__ void tile_coords(int t, const KernelParams& p, int& m
 
 __device__ __forceinline__ void record_timeout(unsigned site) { atomicCAS(&g_status, 0u, site); }
 
+// The bounds-check build tests an access before making it; a failed test
+// records its site (first writer wins), raises the CTA's abort flag (every
+// bounded wait then gives up) and the caller skips the access.  Without
+// TCGEMM_CHECK the test is the constant true and vanishes.
+#ifdef TCGEMM_CHECK
+__device__ __forceinline__ bool bounds_ok(bool ok, unsigned site, volatile int* abort_flag) {
+    if (ok) return true;
+    record_timeout(site);
+    *abort_flag = 1;
+    return false;
+}
+#define TC_CHECK(cond, site) bounds_ok((cond), (site), abort_flag)
+#else
+#define TC_CHECK(cond, site) true
+#endif
+
 constexpr int kPartialFloats = kBM * 256;  // one CTA's fp32 partial tile (up to 128 x 256) in the workspace
+constexpr int kMaxSkCtas = 1024;           // CTAs whose flags the workspace's fixed flag area holds (4 each)
 
 // The units of work of one cluster (a CTA pair, or a single CTA): its share
 // of the stream-K iterations first, then its data-parallel tiles c,

@@ -12,6 +12,12 @@
 
 #include "add_matrices.h"
 #include "gemm_f16.h"
+#ifdef TCGEMM_TRACE
+#include "gemm_f16_trace.h"
+#endif
+#ifdef TCGEMM_CHECK
+#include "gemm_f16_check.h"
+#endif
 #include "add_kernel.cuh"
 #include "gemm_kernel.cuh"
 #include "gemm_pair_kernel.cuh"
@@ -155,7 +161,6 @@ int max_slots_for_pair(int out_dtype, int step_k, int pair_m) {
 // CTA.  The flag area has the same size in every plan, so a flag word never
 // lies where another plan keeps a partial tile: it only ever holds 0 or the
 // epoch of some launch.
-constexpr int kMaxSkCtas = 1024;
 constexpr size_t kFlagBytes = (size_t)kMaxSkCtas * 4 * sizeof(unsigned);  // 16 KiB
 
 constexpr size_t workspace_for(int ctas) { return kFlagBytes + (size_t)ctas * kPartialFloats * sizeof(float); }
@@ -604,6 +609,27 @@ gemm_config current_config() {
     return g_cfg;
 }
 
+#ifdef TCGEMM_TRACE
+// The trace build's buffer (gemm_f16_trace_buffer) and its launch count.
+struct TraceState {
+    unsigned long long* buf = nullptr;
+    int slots = 0, ctas = 0, events = 0;
+    unsigned long long launches = 0;
+};
+TraceState g_trace;
+std::mutex g_trace_mu;
+
+// Where this launch records (NULL: not traced), advancing the launch count.
+unsigned long long* next_trace_slot(int* ctas, int* events) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!g_trace.buf) return nullptr;
+    const unsigned long long slot = g_trace.launches++ % (unsigned long long)g_trace.slots;
+    *ctas = g_trace.ctas;
+    *events = g_trace.events;
+    return g_trace.buf + slot * (unsigned long long)g_trace.ctas * kTraceRoles * g_trace.events * 2;
+}
+#endif
+
 // Encode the tensor maps and launch one planned problem (arguments already
 // checked; `plan` made with `cfg` for this device; the workspace, if the plan
 // uses one, large enough).
@@ -648,6 +674,9 @@ int launch_planned(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int
     kp.sk_tiles = plan.sk_tiles;
     kp.sk_pairs = plan.sk_pairs;
     kp.c_in = accumulate ? C : nullptr;
+#ifdef TCGEMM_TRACE
+    kp.trace = next_trace_slot(&kp.trace_ctas, &kp.trace_events);
+#endif
     if (plan.sk_tiles > 0) {
         // flags first, then the partial tiles (layout of workspace_for)
         unsigned e = ++g_epoch;
@@ -810,6 +839,109 @@ int gemm_f16_device_status(int* site, int reset) {
 }
 
 int gemm_f16_abi_version(void) { return 1; }
+
+}  // extern "C"
+
+#ifdef TCGEMM_CHECK
+namespace {
+
+// Every access a launch of plan `p` makes, at the granularity the kernels
+// test them (bounds.cuh): ring slots and their barriers, staging buffers,
+// accumulators, split-K blocks, workspace slots.  Returns the first failing
+// site, 0 if none.  L: the kernel's layout; pair: the CTA-pair kernel.
+template <class L, bool kPair>
+unsigned check_layout(const gemm_plan& p, int acc_cols, int out_cols) {
+    const int S = p.slots;
+    if (S < 1 || S > kMaxStages) return kSiteSmemBounds;  // full[] and empty[] hold kMaxStages
+    const Carve cv = carve(S, L::kABytes, L::kBBytes, L::kStagingBytes, L::kNumBars);
+    // the carve-up, after the worst alignment skip, within the shared memory requested
+    if (cv.end + kMaxAlignSkip > (uint32_t)p.smem_bytes) return kSiteSmemBounds;
+    const uint32_t ring_a = (uint32_t)S * L::kABytes, ring_b = (uint32_t)S * L::kBBytes;
+    const uint32_t staging_all = 4u * 2u * L::kStagingBytes, bars = (uint32_t)L::kNumBars * 8u;
+    for (int st = 0; st < S; ++st) {
+        const int rs = (st - p.release + S) % S;
+        if (!(holds(cv.bar, bars, cv.bar + 8u * st, 8) && holds(cv.bar, bars, cv.bar + 8u * (kMaxStages + st), 8) &&
+              holds(cv.bar, bars, cv.bar + 8u * (kMaxStages + rs), 8) &&
+              holds(cv.a, ring_a, cv.a + st * L::kABytes, L::kABytes) &&
+              holds(cv.b, ring_b, cv.b + st * L::kBBytes, L::kBBytes)))
+            return kSiteSmemBounds;
+    }
+    for (int q = 0; q < 4; ++q)
+        if (!holds(cv.c, staging_all, cv.c + (uint32_t)(q * 2 * L::kStagingBytes), 2 * L::kStagingBytes))
+            return kSiteSmemBounds;
+    // Tensor Memory: an allocation is a power of two from 32 to 512 columns,
+    // the one the plan reports, and holds both accumulators
+    const int tc = L::kTmemCols;
+    if (tc < 32 || tc > 512 || (tc & (tc - 1)) || tc != p.tmem_cols || 2 * acc_cols > tc) return kSiteTmemBounds;
+    if (!kPair && p.split > 1) {
+        const int chunks = p.tile_n / out_cols;
+        const uint32_t block = (uint32_t)(out_cols / 4 * 32 * 16);
+        const bool to_staging = (chunks + 1) / 2 * block <= 2u * L::kStagingBytes;
+        for (int c = 0; c < chunks; ++c)
+            for (int q = 0; q < 4; ++q) {
+                const bool ok = p.split == 2 && to_staging
+                                    ? holds(cv.c, staging_all, cv.c + push_offset(c, q, block, L::kStagingBytes), block)
+                                    : holds(cv.a, ring_a + ring_b, cv.a + park_offset(c, q, block), block);
+                if (!ok) return kSiteSmemBounds;
+            }
+    }
+    if (p.sk_tiles > 0) {
+        const long long ctas = (long long)p.sk_pairs * (kPair ? 2 : 1);
+        if (ctas > kMaxSkCtas || (size_t)p.workspace_bytes < workspace_for((int)ctas)) return kSiteWorkspaceBounds;
+        // a partial of up to 128 x (accumulator columns x lanes folded) fp32 per CTA
+        if ((long long)kBM * acc_cols > kPartialFloats) return kSiteWorkspaceBounds;
+    }
+    return 0;
+}
+
+}  // namespace
+
+extern "C" int gemm_f16_check_plan(const gemm_plan* plan, int out_dtype, int* site) {
+    if (!plan || !site) return GEMM_ERR_NULL;
+    *site = 0;
+    if (out_dtype != GEMM_OUT_F16 && out_dtype != GEMM_OUT_F32) return GEMM_ERR_DTYPE;
+    const gemm_plan& p = *plan;
+    const bool f16 = out_dtype == GEMM_OUT_F16;
+    unsigned s = kSiteSmemBounds;  // a plan no kernel runs
+    if (p.cta_group == 2 && p.tile_m == 128 && p.tile_n == 128 && p.tile_k == 128)
+        s = f16 ? check_layout<PairLayout<0, 128, 128, 128>, true>(p, 64, 64)
+                : check_layout<PairLayout<1, 128, 128, 128>, true>(p, 64, 32);
+    else if (p.cta_group == 2 && p.tile_m == 256 && p.tile_n == 256 && p.tile_k == 128)
+        s = f16 ? check_layout<PairLayout<0, 128>, true>(p, 256, 64) : check_layout<PairLayout<1, 128>, true>(p, 256, 32);
+    else if (p.cta_group == 2 && p.tile_m == 256 && p.tile_n == 256 && p.tile_k == 64)
+        s = f16 ? check_layout<PairLayout<0, 64>, true>(p, 256, 64) : check_layout<PairLayout<1, 64>, true>(p, 256, 32);
+    else if (p.cta_group == 1 && p.tile_m == 128 && p.tile_k == 64 && p.tile_n == 256)
+        s = f16 ? check_layout<Layout<256, 0>, false>(p, 256, 64) : check_layout<Layout<256, 1>, false>(p, 256, 32);
+    else if (p.cta_group == 1 && p.tile_m == 128 && p.tile_k == 64 && p.tile_n == 128)
+        s = f16 ? check_layout<Layout<128, 0>, false>(p, 128, 64) : check_layout<Layout<128, 1>, false>(p, 128, 32);
+    else if (p.cta_group == 1 && p.tile_m == 128 && p.tile_k == 64 && p.tile_n == 64)
+        s = f16 ? check_layout<Layout<64, 0>, false>(p, 64, 64) : check_layout<Layout<64, 1>, false>(p, 64, 32);
+    *site = (int)s;
+    return s == 0 ? GEMM_OK : GEMM_ERR_CONFIG;
+}
+#endif
+
+extern "C" {
+
+#ifdef TCGEMM_TRACE
+int gemm_f16_trace_buffer(void* buffer, size_t bytes, int launch_slots, int ctas, int events) {
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!buffer) {
+        g_trace = TraceState();
+        return GEMM_OK;
+    }
+    if (launch_slots < 1 || ctas < 1 || events < 1) return GEMM_ERR_NULL;
+    if ((uintptr_t)buffer & 7) return GEMM_ERR_ALIGN;
+    const unsigned long long need = (unsigned long long)launch_slots * ctas * kTraceRoles * events * 16ull;
+    if (bytes < need) return GEMM_ERR_NULL;
+    g_trace.buf = static_cast<unsigned long long*>(buffer);
+    g_trace.slots = launch_slots;
+    g_trace.ctas = ctas;
+    g_trace.events = events;
+    g_trace.launches = 0;
+    return GEMM_OK;
+}
+#endif
 
 int add_matrices_f32(const float* X, const float* Y, float* Z, int M, int N, gemm_stream_t stream) {
     if (M < 0 || N < 0) return GEMM_ERR_DIM;

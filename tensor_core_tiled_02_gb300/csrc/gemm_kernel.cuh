@@ -87,13 +87,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
     const int S = p.slots;
-    const uint32_t sA = base;
-    const uint32_t sB = sA + S * L::kABytes;
-    const uint32_t sC = sB + S * L::kBBytes;
-    const uint32_t bar0 = sC + 4 * 2 * L::kStagingBytes;
-    const uint32_t misc_off = (bar0 - base) + L::kNumBars * 8;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + misc_off);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + misc_off + 4);
+    const Carve cv = carve(S, L::kABytes, L::kBBytes, L::kStagingBytes, L::kNumBars);
+    const uint32_t sA = base + cv.a;
+    const uint32_t sB = base + cv.b;
+    const uint32_t sC = base + cv.c;
+    const uint32_t bar0 = base + cv.bar;
+#ifdef TCGEMM_CHECK
+    // the carve-up fits the shared memory this launch has, checked before any
+    // of it is written (every CTA of the launch decides alike, so none is left
+    // waiting on another)
+    if ((base - raw) + cv.end > ptx::dynamic_smem_size()) {
+        if (threadIdx.x == 0) record_timeout(kSiteSmemBounds);
+        return;
+    }
+#endif
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + cv.misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + cv.misc + 4);
+    // the parts of the carve-up, for the bounds-check build's tests
+    const uint32_t ring_a = (uint32_t)S * L::kABytes, ring_b = (uint32_t)S * L::kBBytes;
+    const uint32_t staging_all = 4u * 2u * L::kStagingBytes, bars = (uint32_t)L::kNumBars * 8u;
+    (void)ring_a, (void)ring_b, (void)staging_all, (void)bars;
 
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
@@ -107,17 +120,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // block of kCols / 4 column groups x 32 rows x 16 bytes in the ring
     constexpr int kChunks = BN / kCols;
     constexpr uint32_t kWarpChunkBytes = kCols / 4 * 32 * 16;
-    auto park_at = [&](int c, int qd) { return sA + (uint32_t)(c * 4 + qd) * kWarpChunkBytes; };
+    auto park_at = [&](int c, int qd) { return sA + park_offset(c, qd, kWarpChunkBytes); };
     // split 2: the blocks a warp receives (its share of at most ceil(chunks / 2)
     // chunks) fit its two staging buffers for tiles up to 128 columns
     constexpr bool kPushToStaging = (kChunks + 1) / 2 * kWarpChunkBytes <= 2 * L::kStagingBytes;
     auto push_slot = [&](int c, int qd) {  // where chunk c's block of warp qd lands in its owner
-        return kPushToStaging ? sC + (uint32_t)(qd * 2 * L::kStagingBytes) + (uint32_t)(c / 2) * kWarpChunkBytes
-                              : park_at(c, qd);
+        return kPushToStaging ? sC + push_offset(c, qd, kWarpChunkBytes, L::kStagingBytes) : park_at(c, qd);
     };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    Tracer tr(p, warp);  // warp w records as role w (trace build only)
+    if (lane == 0) tr(kTrEntry, ptx::smid());
     const int split = p.split;
     const uint32_t rank = split > 1 ? ptx::cluster_ctarank() : 0u;
     // split-K: the chunks this rank owns
@@ -158,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (split > 1) ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (lane == 0) tr(kTrSetup);
 
     // this CTA's cluster (itself without split-K) and the clusters of the grid
     const int cl = blockIdx.x / split;
@@ -189,6 +204,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool rev = split == 1 && k0 == 0 && k1 == p.k_blocks && (u.ndp & 1) == 0;
                 for (int kb0 = k0; kb0 < k1; ++kb0) {
                     const int kb = rev ? k1 - 1 - (kb0 - k0) : kb0;
+                    if (!TC_CHECK(holds(bar0, bars, empty_bar(stage), 8) && holds(bar0, bars, full_bar(stage), 8) &&
+                                      holds(sA, ring_a, sA + stage * L::kABytes, L::kABytes) &&
+                                      holds(sB, ring_b, sB + stage * L::kBBytes, L::kBBytes),
+                                  kSiteSmemBounds)) {
+                        ok = false;
+                        break;
+                    }
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -199,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the previous kernel's writes of A and B are done from here on
                         ptx::grid_dependency_wait();
                         ptx::grid_launch_dependents();
+                        tr(kTrDepWait);
                         dep_done = true;
                     }
                     ptx::tma_load_2d(sA + stage * L::kABytes, &tmA, fb, kb * kBK, mb * kBM);
@@ -206,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < BN / 64; ++j)
                         ptx::tma_load_2d(sB + stage * L::kBBytes + j * kBoxBytes, &tmB, fb, nb * BN + j * 64,
                                          kb * kBK);
+                    tr(kTrLoad, kb);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -243,13 +267,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
+                if (!TC_CHECK((uint32_t)(acc * BN + BN) <= (uint32_t)L::kTmemCols, kSiteTmemBounds)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
                 for (int kb = k0; kb < k1; ++kb) {
+                    int rs = stage - p.release;
+                    if (rs < 0) rs += S;
+                    if (!TC_CHECK(holds(bar0, bars, full_bar(stage), 8) && holds(bar0, bars, empty_bar(rs), 8) &&
+                                      holds(sA, ring_a, sA + stage * L::kABytes, L::kABytes) &&
+                                      holds(sB, ring_b, sB + stage * L::kBBytes, L::kBBytes),
+                                  kSiteSmemBounds)) {
+                        ok = false;
+                        break;
+                    }
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
+                    tr(kTrFull, kb);
                     const uint32_t a0 = sA + stage * L::kABytes;
                     const uint32_t b0 = sB + stage * L::kBBytes;
 #pragma unroll
@@ -262,11 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::mma_f16_ss(d_tmem, ad, bd, idesc, (kb != k0) || (k != 0));
                     }
                     // release the slot `release` steps back once these MMAs are done
-                    if (it >= p.release) {
-                        int rs = stage - p.release;
-                        if (rs < 0) rs += S;
-                        ptx::mma_commit(empty_bar(rs));
-                    }
+                    if (it >= p.release) ptx::mma_commit(empty_bar(rs));
                     ++it;
                     if (++stage == S) {
                         stage = 0;
@@ -275,6 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 ptx::mma_commit(tfull_bar(acc));
+                tr(kTrTileDone, t);
             }
             // every MMA this thread issued completes before TMEM is freed
             ptx::mma_commit(drain_bar);
@@ -307,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // are done from here on
             ptx::grid_dependency_wait();
             ptx::grid_launch_dependents();
+            if (lane == 0) tr(kTrDepWait);
         }
         UnitIter u;
         unit_iter_init(u, p, cl, clusters);
@@ -318,6 +354,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
+            // bounds-check build: everything this unit's drain touches (this warp's
+            // staging, both accumulators' columns, the split-K blocks, the
+            // workspace slot and flags)
+            bool in_bounds = TC_CHECK(holds(sC, staging_all, staging, 2 * L::kStagingBytes), kSiteSmemBounds) &&
+                             TC_CHECK(2u * BN <= (uint32_t)L::kTmemCols, kSiteTmemBounds);
+            for (int c = 0; in_bounds && split == 2 && c < kChunks; ++c)
+                in_bounds = TC_CHECK(kPushToStaging ? holds(sC, staging_all, push_slot(c, q), kWarpChunkBytes)
+                                                    : holds(sA, ring_a + ring_b, push_slot(c, q), kWarpChunkBytes),
+                                     kSiteSmemBounds);
+            for (int c = 0; in_bounds && split > 2 && c < kChunks; ++c)
+                in_bounds = TC_CHECK(holds(sA, ring_a + ring_b, park_at(c, q), kWarpChunkBytes), kSiteSmemBounds);
+            if (in_bounds && split == 1 && p.sk_tiles > 0)
+                in_bounds = TC_CHECK(cl < p.sk_pairs && cl < kMaxSkCtas, kSiteWorkspaceBounds);
+            if (!in_bounds) break;
             // Dry pass first (see dry_ok): everything the code below does once
             // the accumulator is ready, on the other accumulator, with no store,
             // no push and no hand-back; the real pass then finds the code in the
@@ -330,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the previous kernel's reads and writes of C are done from here on
                     ptx::grid_dependency_wait();
                     ptx::grid_launch_dependents();
+                    if (lane == 0) tr(kTrDepWait);
                 }
                 if (has_k && !dry) {
                     // a legitimate wait here spans a whole tile's main loop: allow 4x
@@ -338,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after();
+                    if (lane == 0) tr(kTrAccReady, t);
                 }
                 const int row0 = mb * kBM + q * 32;
                 // the dry pass reads the other accumulator, which a CTA holding one tile never writes
@@ -377,12 +429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                  ptx::mapa(red_data_bar, peer));
                         }
                     }
+                    if (!dry && lane == 0) tr(kTrPushed);
                     // the partner's blocks of this CTA's chunks
                     if (!dry && owned > 0 &&
                         !warp_wait<true>(red_data_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceData, lane)) {
                         failed = true;
                         break;
                     }
+                    if (!dry && lane == 0) tr(kTrPartner);
                     // done with the partner: its pushes have landed here, and it arrives
                     // only once this CTA's pushes have landed there
                     if (!dry) {
@@ -407,13 +461,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     __syncwarp();
-                    if (lane == 0)
+                    if (lane == 0) {
                         for (int r = 0; r < split; ++r)
                             if (r != (int)rank) ptx::mbar_arrive_cluster(ptx::mapa(red_ready_bar, (uint32_t)r));
+                        tr(kTrPushed);
+                    }
                     if (!warp_wait<true>(red_ready_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceReady, lane)) {
                         failed = true;
                         break;
                     }
+                    if (lane == 0) tr(kTrPartner);
                 } else if (k0 > 0) {
                     // stream-K contributor: park this CTA's partial in its workspace
                     // slot as [column / 4][row] 16-byte groups (consecutive lanes,
@@ -434,7 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
                     __threadfence();
                     __syncwarp();
-                    if (lane == 0) ptx::st_release_gpu(p.flags + cl * 4 + q, p.epoch);
+                    if (lane == 0) {
+                        ptx::st_release_gpu(p.flags + cl * 4 + q, p.epoch);
+                        tr(kTrParked, t);
+                    }
                     continue;
                 }
                 // stream-K owner: the CTAs after this one whose shares start inside
@@ -458,8 +518,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // every lane has acquired them: hand the flags back (zero), so a later
                     // launch with the same epoch (a replayed CUDA graph) waits afresh
                     __syncwarp();
-                    if (lane == 0)
+                    if (lane == 0) {
                         for (int qq = cl + 1; qq < q_end; ++qq) ptx::st_relaxed_gpu(p.flags + qq * 4 + q, 0u);
+                        tr(kTrFlags, t);
+                    }
                 }
 
 #pragma unroll 1
@@ -521,6 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     add_c_in<OUT>(v, p, dry ? p.M : row0 + lane, nb * BN + c * kCols);  // row M: nothing read
                     store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, dry ? p.M : row0,
                                      dry && p.M > (1 << 30));
+                    if (!dry && lane == 0) tr(kTrStored, c);
                     if (dry) {
                         // one chunk runs all of the loop's code; the staging is free
                         // again and the real pass starts on buffer 0 (under split-K
@@ -543,7 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (split == 2 && owned > 0 && warp == 2 && lane == 0) wait_drain(red_data_bar, 0, p.wait_limit);
         // the staging buffers must have been read before shared memory goes
         // away; the global writes themselves complete with the grid
-        if (lane == 0) ptx::bulk_wait_group_read<0>();
+        if (lane == 0) {
+            ptx::bulk_wait_group_read<0>();
+            tr(kTrStoreRead);
+        }
         __syncwarp();
         if (split > 1 && !arrived) ptx::cluster_arrive();
     }
@@ -553,6 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // split-K: no rank leaves while another may still read or write its
     // shared memory or arrive on its barriers
     if (split > 1) ptx::cluster_wait();
+    if (lane == 0) tr(kTrExit);
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();

@@ -92,13 +92,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
     const int S = p.slots;
-    const uint32_t sA = base;
-    const uint32_t sB = sA + S * L::kABytes;
-    const uint32_t sC = sB + S * L::kBBytes;
-    const uint32_t bar0 = sC + 4 * 2 * L::kStagingBytes;
-    const uint32_t misc_off = (bar0 - base) + L::kNumBars * 8;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + misc_off);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + misc_off + 4);
+    const Carve cv = carve(S, L::kABytes, L::kBBytes, L::kStagingBytes, L::kNumBars);
+    const uint32_t sA = base + cv.a;
+    const uint32_t sB = base + cv.b;
+    const uint32_t sC = base + cv.c;
+    const uint32_t bar0 = base + cv.bar;
+#ifdef TCGEMM_CHECK
+    // the carve-up fits the shared memory this launch has, checked before any
+    // of it is written (both CTAs of every pair decide alike)
+    if ((base - raw) + cv.end > ptx::dynamic_smem_size()) {
+        if (threadIdx.x == 0) record_timeout(kSiteSmemBounds);
+        return;
+    }
+#endif
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(base_ptr + cv.misc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base_ptr + cv.misc + 4);
+    // the parts of the carve-up, for the bounds-check build's tests
+    const uint32_t ring_a = (uint32_t)S * L::kABytes, ring_b = (uint32_t)S * L::kBBytes;
+    const uint32_t staging_all = 4u * 2u * L::kStagingBytes, bars = (uint32_t)L::kNumBars * 8u;
+    (void)ring_a, (void)ring_b, (void)staging_all, (void)bars;
 
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
@@ -109,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    Tracer tr(p, warp);  // warp w records as role w (trace build only)
+    if (lane == 0) tr(kTrEntry, ptx::smid());
     const uint32_t rank = ptx::cluster_ctarank();  // 0: leader (issues the MMAs), 1: peer
 
     if (threadIdx.x == 0) {
@@ -140,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::cluster_sync();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    if (lane == 0) tr(kTrSetup);
 
     const int cluster = blockIdx.x >> 1;   // this pair
     const int clusters = gridDim.x >> 1;
@@ -167,6 +182,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool rev = k0 == 0 && k1 == KB && (u.ndp & 1) == 0;
                 for (int kb0 = k0; kb0 < k1; ++kb0) {
                     const int kb = rev ? k1 - 1 - (kb0 - k0) : kb0;
+                    if (!TC_CHECK(holds(bar0, bars, empty_bar(stage), 8) && holds(bar0, bars, full_bar(stage), 8) &&
+                                      holds(sA, ring_a, sA + stage * L::kABytes, L::kABytes) &&
+                                      holds(sB, ring_b, sB + stage * L::kBBytes, L::kBBytes),
+                                  kSiteSmemBounds)) {
+                        ok = false;
+                        break;
+                    }
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit, kSiteProducerEmpty)) {
                         ok = false;
                         break;
@@ -178,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // the previous kernel's writes of A and B are done from here on
                         ptx::grid_dependency_wait();
                         ptx::grid_launch_dependents();
+                        tr(kTrDepWait);
                         dep_done = true;
                     }
 #pragma unroll
@@ -188,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < L::kBBoxes; ++j)
                         ptx::tma_load_2d_pair(sB + stage * L::kBBytes + j * L::kBBoxBytes, &tmB, fb, n0 + j * 64,
                                               kb * SK);
+                    tr(kTrLoad, kb);
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                     if (++stage == S) {
@@ -223,13 +247,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ptx::tc_fence_after();
+                if (!TC_CHECK((uint32_t)(acc * L::kAccCols + L::kAccCols) <= (uint32_t)L::kTmemCols, kSiteTmemBounds)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * L::kAccCols);
                 for (int kb = k0; kb < k1; ++kb) {
+                    int rs = stage - p.release;
+                    if (rs < 0) rs += S;
+                    if (!TC_CHECK(holds(bar0, bars, full_bar(stage), 8) && holds(bar0, bars, empty_bar(rs), 8) &&
+                                      holds(sA, ring_a, sA + stage * L::kABytes, L::kABytes) &&
+                                      holds(sB, ring_b, sB + stage * L::kBBytes, L::kBBytes),
+                                  kSiteSmemBounds)) {
+                        ok = false;
+                        break;
+                    }
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
+                    tr(kTrFull, kb);
                     const uint32_t a0 = sA + stage * L::kABytes;
                     const uint32_t b0 = sB + stage * L::kBBytes;
                     // descriptors of the step's first K slice; later slices add to
@@ -245,11 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bd = bd0 + (uint64_t)((k * (kUmmaK * 128)) >> 4);
                         ptx::mma_f16_ss_pair(d_tmem, ad, bd, idesc, (kb != k0) || (k != 0));
                     }
-                    if (it >= p.release) {
-                        int rs = stage - p.release;
-                        if (rs < 0) rs += S;
-                        ptx::mma_commit_pair_multicast(empty_bar(rs), 0x3);
-                    }
+                    if (it >= p.release) ptx::mma_commit_pair_multicast(empty_bar(rs), 0x3);
                     ++it;
                     if (++stage == S) {
                         stage = 0;
@@ -258,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok) break;
                 ptx::mma_commit_pair_multicast(tfull_bar(acc), 0x3);
+                tr(kTrTileDone, t);
             }
             ptx::mma_commit_pair(drain_bar);
             wait_drain(drain_bar, 0, p.wait_limit);
@@ -282,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // are done from here on
             ptx::grid_dependency_wait();
             ptx::grid_launch_dependents();
+            if (lane == 0) tr(kTrDepWait);
         }
         UnitIter u;
         unit_iter_init(u, p, cluster, clusters);
@@ -292,6 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
+            // bounds-check build: everything this unit's drain touches (this warp's
+            // staging, both accumulators' columns, the workspace slot and flags)
+            if (!(TC_CHECK(holds(sC, staging_all, staging, 2 * L::kStagingBytes), kSiteSmemBounds) &&
+                  TC_CHECK(2u * L::kAccCols <= (uint32_t)L::kTmemCols, kSiteTmemBounds) &&
+                  TC_CHECK(!(k0 > 0 || k1 < KB) || (cluster < p.sk_pairs && 2 * p.sk_pairs <= kMaxSkCtas),
+                           kSiteWorkspaceBounds)))
+                break;
             const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
             // stream-K owner: the clusters after this one whose units start inside
             // this tile hold the rest of its K range
@@ -312,8 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // every lane has acquired them: hand the flags back (zero), so a later
                 // launch with the same epoch (a replayed CUDA graph) waits afresh
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0) {
                     for (int qq = cluster + 1; qq < q_end; ++qq) ptx::st_relaxed_gpu(p.flags + (qq * 2 + (int)rank) * 4 + q, 0u);
+                    tr(kTrFlags, t);
+                }
                 // the owner unit is its cluster's last, so the other accumulator is
                 // free: sum the contributors' partials into it while the MMAs run
                 UnitIter peek = u;
@@ -362,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // the previous kernel's reads and writes of C are done from here on
                     ptx::grid_dependency_wait();
                     ptx::grid_launch_dependents();
+                    if (lane == 0) tr(kTrDepWait);
                 }
                 if (KB > 0 && !dry) {
                     if (!warp_wait(tfull_bar(acc), aph, abort_flag, 4 * p.wait_limit, kSiteEpilogueTmemFull,
@@ -370,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after();
+                    if (lane == 0) tr(kTrAccReady, t);
                 }
                 if (!dry && k0 > 0) break;  // stream-K contributor: parks its partial below
                 const uint32_t trow = lane_base + (uint32_t)((dry ? acc ^ 1 : acc) * L::kAccCols);
@@ -415,6 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     add_c_in<OUT>(v, p, dry ? p.M : row0 + lane, col0 + c * kCols);  // row M: nothing read
                     store_chunk<OUT>(v, &tmC, staging, nstore, lane, col0 + c * kCols, dry ? p.M : row0,
                                      dry && p.M > (1 << 30));
+                    if (!dry && lane == 0) tr(kTrStored, c);
                     if (dry) {
                         // one chunk runs all of the loop's code; the staging is free again
                         if (lane == 0) ptx::bulk_wait_group_read<0>();
@@ -446,11 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) ptx::st_release_gpu(p.flags + (cluster * 2 + (int)rank) * 4 + q, p.epoch);
+                if (lane == 0) {
+                    ptx::st_release_gpu(p.flags + (cluster * 2 + (int)rank) * 4 + q, p.epoch);
+                    tr(kTrParked, t);
+                }
                 continue;
             }
         }
-        if (lane == 0) ptx::bulk_wait_group_read<0>();
+        if (lane == 0) {
+            ptx::bulk_wait_group_read<0>();
+            tr(kTrStoreRead);
+        }
         __syncwarp();
     }
 
@@ -458,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     // neither CTA leaves while the other may still signal into it
     ptx::cluster_sync();
+    if (lane == 0) tr(kTrExit);
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();

@@ -12,6 +12,26 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Nanoseconds of the GPU-wide timer (the same clock on every SM).
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bytes of dynamic shared memory this CTA was launched with.
+__device__ __forceinline__ uint32_t dynamic_smem_size() {
+    uint32_t s;
+    asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(s));
+    return s;
+}
+
+__device__ __forceinline__ uint32_t smid() {
+    uint32_t s;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(s));
+    return s;
+}
+
 __device__ __forceinline__ uint32_t lane_id() {
     uint32_t l;
     asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));

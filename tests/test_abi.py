@@ -13,6 +13,10 @@ from tensor_core_tiled_02_gb300.synthetic import WORKLOADS
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))]
+# headers of the debug variants: declared only by the library of that variant
+VARIANT_HEADERS = {"trace": os.path.join(ROOT, "include", "gemm_f16_trace.h"),
+                   "check": os.path.join(ROOT, "include", "gemm_f16_check.h")}
+PRODUCT_HEADERS = [h for h in HEADERS if h not in VARIANT_HEADERS.values()]
 
 # status codes, as the header defines them
 OK, NULL, DIM, DTYPE, ALIGN, ALIAS, CONFIG = 0, -1, -2, -3, -4, -5, -6
@@ -25,10 +29,11 @@ def lib():
     return tc.load_library()
 
 
-def declared_functions():
-    """Every function the headers under include/ declare."""
+def declared_functions(headers=None):
+    """Every function the given headers (default: the product's under
+    include/) declare."""
     names = set()
-    for h in HEADERS:
+    for h in headers or PRODUCT_HEADERS:
         text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
         text = re.sub(r"#[^\n]*", "", text)
         names.update(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\([^;{]*\)\s*;", text))
@@ -41,6 +46,25 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert lib.gemm_f16_abi_version() == 1
+    # the product does not carry the debug variants' entry points
+    for v, h in VARIANT_HEADERS.items():
+        for n in declared_functions([h]):
+            assert not hasattr(lib, n), n
+
+
+@pytest.mark.parametrize("variant", sorted(tcbuild.VARIANTS))
+def test_debug_variants_export_the_product_abi_and_their_own(variant):
+    """libtcgemm_trace.so and libtcgemm_check.so (built beside the product)
+    export every product entry point, and the trace build its own."""
+    path = tcbuild.variant_lib(variant)
+    if not os.path.exists(path):
+        tcbuild.build(variant=variant)
+    vlib = ctypes.CDLL(path)
+    names = declared_functions() + (declared_functions([VARIANT_HEADERS[variant]]) if variant in VARIANT_HEADERS
+                                    else [])
+    for n in names:
+        assert hasattr(vlib, n), (variant, n)
+    assert vlib.gemm_f16_abi_version() == 1
 
 
 def test_add_argument_errors_before_any_cuda_call(lib):
