@@ -37,10 +37,12 @@
 //     ring, arrives on the others' `red_ready`, and reads the other ranks'
 //     blocks of its own chunks over distributed shared memory.
 // An owner adds the other ranks' partials to its own in ascending rank order
-// (deterministic) and drains the sum as above.  A cluster barrier, arrived at
-// as soon as a thread is done with the other CTAs and waited on just before
-// leaving, keeps every rank's shared memory and barriers alive while the
-// others may still touch them.  The planner gives each cluster exactly one
+// (deterministic) and drains the sum as above.  The cluster barrier runs two
+// phases: at set-up (every rank's barriers initialised before any remote
+// arrive; only the epilogue waits on it there) and at exit (arrived at as
+// soon as a thread is done with the other CTAs, waited on just before
+// leaving), which keeps every rank's shared memory and barriers alive while
+// the others may still touch them.  The planner gives each cluster exactly one
 // tile in this mode.
 //
 // Stream-K (split = 1, sk_tiles > 0): as in the CTA-pair kernel, the K
@@ -168,8 +170,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // every CTA of the cluster has its barriers initialised before any remote arrive
-    if (split > 1) ptx::cluster_sync();
+    // Every CTA of the cluster has its barriers initialised before any remote
+    // arrive.  The arrival is relaxed (fence.mbarrier_init above released the
+    // initialisation; a release here costs ~1,000 cycles on the way to the
+    // first load).  Only the epilogue, which signals and writes the other CTAs,
+    // waits now; the producer and the MMA issuer touch nothing but their own
+    // CTA and wait just before their second arrival, at the end.
+    if (split > 1) {
+        ptx::cluster_arrive_relaxed();
+        if (warp >= 2) ptx::cluster_wait();
+    }
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (lane == 0) tr(kTrSetup);
@@ -243,8 +253,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < S; ++s)
                 if (issued_mask & (1u << s)) wait_drain(full_bar(s), (issued_phase >> s) & 1u, p.wait_limit);
         }
-        // split-K: the producer never touches another CTA
-        if (split > 1) ptx::cluster_arrive();
+        // split-K: the producer never touches another CTA (the set-up phase of
+        // the cluster barrier completed long ago)
+        if (split > 1) {
+            ptx::cluster_wait();
+            ptx::cluster_arrive();
+        }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0 && has_k) {
@@ -315,7 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(drain_bar);
             wait_drain(drain_bar, 0, p.wait_limit);
         }
-        if (split > 1) ptx::cluster_arrive();
+        if (split > 1) {
+            ptx::cluster_wait();
+            ptx::cluster_arrive();
+        }
     } else {
         // ---------------- epilogue: TMEM -> registers -> SMEM -> TMA store ----------------
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
@@ -430,19 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     if (!dry && lane == 0) tr(kTrPushed);
-                    // the partner's blocks of this CTA's chunks
-                    if (!dry && owned > 0 &&
-                        !warp_wait<true>(red_data_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceData, lane)) {
-                        failed = true;
-                        break;
-                    }
-                    if (!dry && lane == 0) tr(kTrPartner);
-                    // done with the partner: its pushes have landed here, and it arrives
-                    // only once this CTA's pushes have landed there
-                    if (!dry) {
-                        ptx::cluster_arrive();
-                        arrived = true;
-                    }
+                    // the partner's blocks are waited for in the chunk loop below, after
+                    // this CTA's own chunk has come out of TMEM
                 } else if (split > 2) {
                     // park the partial of every chunk another rank owns in this CTA's
                     // ring: this warp's 32 rows as [column / 4][row] 16-byte groups
@@ -544,6 +550,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
                     }
                     if (split == 2) {
+                        if (!dry && !arrived) {
+                            // the partner's blocks of this CTA's chunks
+                            if (!warp_wait<true>(red_data_bar, 0, abort_flag, 4 * p.wait_limit, kSiteReduceData, lane)) {
+                                failed = true;
+                                break;
+                            }
+                            if (lane == 0) tr(kTrPartner);
+                            // done with the partner: its pushes have landed here, and it arrives
+                            // only once this CTA's pushes have landed there (the barrier keeps
+                            // shared memory alive; the data went through mbarriers, so the
+                            // arrival need not release anything)
+                            ptx::cluster_arrive_relaxed();
+                            arrived = true;
+                        }
                         // the partner's partial, pushed into this CTA
                         uint32_t x[kCols];
 #pragma unroll
@@ -594,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                 }
+                if (failed) break;
                 // split-K over two ranks: this CTA's staging is the partner's to push into
                 if (dry && split == 2) {
                     __syncwarp();

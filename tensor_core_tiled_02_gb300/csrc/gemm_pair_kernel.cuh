@@ -150,8 +150,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    // both CTAs' barriers are initialised before either signals the other
-    ptx::cluster_sync();
+    // both CTAs' barriers are initialised before either signals the other (a
+    // relaxed arrival: fence.mbarrier_init above released the initialisation)
+    ptx::cluster_arrive_relaxed();
+    ptx::cluster_wait();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     if (lane == 0) tr(kTrSetup);

@@ -118,6 +118,9 @@ __device__ __forceinline__ void cluster_sync() {
 // The two halves of cluster_sync, for a thread that is done with the other
 // CTAs long before it may leave: arrive (release) early, wait (acquire) late.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+// An arrival that orders nothing (for a barrier that only marks progress, or
+// whose data was released by another fence or went through mbarriers).
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // 16 bytes from registers into another CTA's shared memory; the bytes count as
