@@ -88,6 +88,11 @@ typedef struct {
     int sk_tiles;               /* tiles whose K iterations are shared by clusters (stream-K) */
     int sk_pairs;               /* clusters sharing them: CTA pairs, or single CTAs (cta_group 1) */
     long long workspace_bytes;  /* workspace gemm_f16_ws needs for its stream-K plan; 0 if none */
+    int sk_split;               /* 0: the shared K iterations are dealt out in even contiguous shares;
+                                   > 0 (CTA pairs, a last wave more than half full): pair i runs K steps
+                                   [0, sk_split) of shared tile i, and the idle pairs ("helpers") run
+                                   steps [sk_split, k_steps) of the shared tiles, one after another */
+    int sk_helper_tiles;        /* with sk_split > 0: shared tiles each helper pair runs */
 } gemm_plan;
 
 /* Tuning override.  Zero in a field means "planner default". */
@@ -262,7 +267,7 @@ const char *gemm_f16_strerror(int code);
  */
 int gemm_f16_device_status(int *site, int reset);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2 (gemm_plan gained sk_split and sk_helper_tiles). */
 int gemm_f16_abi_version(void);
 
 #ifdef __cplusplus

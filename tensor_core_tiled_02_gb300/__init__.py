@@ -42,7 +42,8 @@ class GemmPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "cta_group", "tile_m", "tile_n", "tile_k", "tiles_m", "tiles_n", "num_tiles", "k_steps", "stages",
         "release", "slots", "split", "grid", "raster_group", "smem_bytes", "tmem_cols", "threads",
-        "dp_tiles", "sk_tiles", "sk_pairs")] + [("workspace_bytes", ctypes.c_longlong)]
+        "dp_tiles", "sk_tiles", "sk_pairs")] + [("workspace_bytes", ctypes.c_longlong)] + [
+        (n, ctypes.c_int) for n in ("sk_split", "sk_helper_tiles")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}

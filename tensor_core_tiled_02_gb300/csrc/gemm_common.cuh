@@ -50,10 +50,16 @@ struct KernelParams {
     long long wait_limit;  // clock cycles a single wait may take before giving up
     int inject;            // test hook: 1 = the producer issues no loads at all
     // stream-K: tiles [0, dp_tiles) run data-parallel; the K iterations of
-    // the remaining sk_tiles are shared evenly by the first sk_pairs clusters
-    // (CTA pairs, or single CTAs in the one-CTA kernel), partial tiles meeting
-    // through `ws` and `flags`
+    // the remaining sk_tiles are shared by the first sk_pairs clusters (CTA
+    // pairs, or single CTAs in the one-CTA kernel), partial tiles meeting
+    // through `ws` and `flags`.  sk_split 0: even contiguous shares.
+    // sk_split > 0 (helpers, CTA pairs only): cluster c < sk_tiles runs K
+    // steps [0, sk_split) of shared tile c; the H = sk_pairs - sk_tiles
+    // clusters after them are helpers, helper h running steps [sk_split,
+    // k_blocks) of shared tiles h, h + H, h + 2H, ... (at most sk_helper_tiles
+    // of them), one unit each
     int dp_tiles, sk_tiles, sk_pairs;
+    int sk_split, sk_helper_tiles;
     unsigned epoch;        // value a flag takes when its partial is ready in this launch
     float* ws;             // one 128 x 256 fp32 partial per CTA of the sharing clusters
     unsigned* flags;       // one flag per epilogue warp of those CTAs
@@ -191,12 +197,17 @@ constexpr int kMaxSkCtas = 1024;           // CTAs whose flags the workspace's f
 // c + clusters, ... below dp_tiles.  Running the shares first keeps every
 // sharing cluster on the same K range at the same time, and an owner unit's
 // wait for its contributors' partials, and their reduction, overlap the
-// cluster's next tile instead of ending the launch.  Producer, MMA issuer and
-// epilogue walk the same sequence.
+// cluster's next tile instead of ending the launch.  Under helper stream-K
+// the main units (steps [0, sk_split) of one shared tile each) run in step
+// with one another, and so do the helpers (steps [sk_split, k_blocks) of one
+// tile after another, the helpers' j-th tiles being H consecutive ones): at
+// any time two K ranges are in use, whose operand blocks the sharing pairs
+// find in L2.  Producer, MMA issuer and epilogue walk the same sequence.
 struct UnitIter {
     int next_dp, stride;
-    long long it, it_end;
-    int ndp;  // data-parallel units handed out so far
+    long long it, it_end;  // even shares: flat (tile, K step) iterations; main, helper: local tile indices
+    int ndp;      // data-parallel units handed out so far
+    int sk_kind;  // 0 even share, 1 main unit, 2 helper units (local tiles it, it + H, ...)
 };
 
 // First stream-K iteration of cluster c: the sk_tiles * k_blocks iterations
@@ -209,16 +220,33 @@ __device__ __forceinline__ void unit_iter_init(UnitIter& u, const KernelParams& 
     u.next_dp = c;
     u.stride = clusters;
     u.ndp = 0;
+    u.sk_kind = 0;
+    u.it = u.it_end = 0;
     if (p.sk_tiles > 0 && c < p.sk_pairs) {
-        u.it = sk_begin(p, c);
-        u.it_end = sk_begin(p, c + 1);
-    } else {
-        u.it = u.it_end = 0;
+        if (p.sk_split == 0) {
+            u.it = sk_begin(p, c);
+            u.it_end = sk_begin(p, c + 1);
+        } else if (c < p.sk_tiles) {
+            u.sk_kind = 1;
+            u.it = c;
+            u.it_end = c + 1;
+        } else {
+            u.sk_kind = 2;
+            u.it = c - p.sk_tiles;
+            u.it_end = p.sk_tiles;
+        }
     }
 }
 
 __device__ __forceinline__ void sk_unit(UnitIter& u, const KernelParams& p, int& tile, int& k0, int& k1) {
     const int KB = p.k_blocks;
+    if (u.sk_kind != 0) {
+        tile = p.dp_tiles + (int)u.it;
+        k0 = u.sk_kind == 1 ? 0 : p.sk_split;
+        k1 = u.sk_kind == 1 ? p.sk_split : KB;
+        u.it += u.sk_kind == 1 ? 1 : p.sk_pairs - p.sk_tiles;
+        return;
+    }
     const int local = (int)(u.it / KB);
     k0 = (int)(u.it - (long long)local * KB);
     const long long left = u.it_end - u.it;
@@ -226,6 +254,30 @@ __device__ __forceinline__ void sk_unit(UnitIter& u, const KernelParams& p, int&
     tile = p.dp_tiles + local;
     u.it += k1 - k0;
 }
+
+// Workspace slot of the partial a contributor unit of tile t parks (cluster
+// c's, which runs that unit): its cluster under even shares, the tile under
+// helpers (a helper contributes to several tiles, each tile has one helper).
+__device__ __forceinline__ int sk_park_slot(const KernelParams& p, int c, int t) {
+    return p.sk_split > 0 ? t - p.dp_tiles : c;
+}
+
+// Slots [first, end) whose partials the owner unit of tile t (cluster c's)
+// adds to its own, in this order: under even shares the following clusters
+// whose shares start inside the tile, under helpers the tile's one slot.
+__device__ __forceinline__ void sk_owner_slots(const KernelParams& p, int c, int t, int& first, int& end) {
+    if (p.sk_split > 0) {
+        first = t - p.dp_tiles;
+        end = first + 1;
+        return;
+    }
+    first = end = c + 1;
+    const long long tile_end = (long long)(t - p.dp_tiles + 1) * p.k_blocks;
+    while (end < p.sk_pairs && sk_begin(p, end) < tile_end) ++end;
+}
+
+// Workspace slots of this plan (partials of CTA pairs take two each).
+__device__ __forceinline__ int sk_slots(const KernelParams& p) { return p.sk_split > 0 ? p.sk_tiles : p.sk_pairs; }
 
 // Next unit: tile id and K-step range [k0, k1).  False when none is left.
 __device__ __forceinline__ bool unit_next(UnitIter& u, const KernelParams& p, int& tile, int& k0, int& k1) {
@@ -306,21 +358,17 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// One 128-byte-wide column chunk of a warp's 32 output rows: convert, write
-// to the warp's staging buffer in the 128-byte swizzle the C tensor map
+// One 128-byte-wide column chunk of a warp's 32 output rows into staging
+// buffer `stg` (4 KiB, 1024-byte aligned) that no earlier store of this warp
+// still reads: convert, write it in the 128-byte swizzle the C tensor map
 // expects (16-byte chunk j of row `lane` at chunk j ^ (lane % 8)), fence for
-// the async proxy and TMA-store it.  Staging is double-buffered per warp.
-// skip_store: everything but the TMA store itself (and nstore stays).  A dry
-// pass through the drain normally stores instead to rows from M on, which
-// the tensor map clips entirely: no byte of C is written.
+// the async proxy and TMA-store it.  skip_store: everything but the TMA store
+// itself.  Returns whether a store was issued.  The last tile of a CTA drains
+// through its idle operand ring, one buffer per chunk and nothing waited for
+// (store_chunk with a ring buffer).
 template <int OUT>
-__device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 32], const CUtensorMap* tmC,
-                                            uint32_t staging, int& nstore, int lane, int x, int y,
-                                            bool skip_store = false) {
-    const uint32_t stg = staging + (uint32_t)((nstore & 1) * 4096);
-    // the store issued from this buffer two rounds ago must have read it
-    if (lane == 0) ptx::bulk_wait_group_read<1>();
-    __syncwarp();
+__device__ __forceinline__ bool stage_and_store(const uint32_t (&v)[OUT == 0 ? 64 : 32], const CUtensorMap* tmC,
+                                                uint32_t stg, int lane, int x, int y, bool skip_store = false) {
     const uint32_t row_addr = stg + lane * 128;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -340,12 +388,31 @@ __device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    if (skip_store) return;
+    if (skip_store) return false;
     if (lane == 0) {
         ptx::tma_store_2d(tmC, stg, x, y);
         ptx::bulk_commit_group();
     }
-    ++nstore;
+    return true;
+}
+
+// stage_and_store through the warp's two staging buffers in turn (nstore
+// counts its stores), waiting first for the store issued from the buffer two
+// rounds ago to have read it; or, with ring_buf != 0, through that buffer of
+// the idle operand ring, waiting for nothing (the same instructions either
+// way, so a dry pass through one warms the other).  skip_store: everything but
+// the TMA store itself (and nstore stays).  A dry pass through the drain
+// normally stores instead to rows from M on, which the tensor map clips
+// entirely: no byte of C is written.
+template <int OUT>
+__device__ __forceinline__ void store_chunk(const uint32_t (&v)[OUT == 0 ? 64 : 32], const CUtensorMap* tmC,
+                                            uint32_t staging, int& nstore, int lane, int x, int y,
+                                            bool skip_store = false, uint32_t ring_buf = 0) {
+    const uint32_t stg = ring_buf != 0 ? ring_buf : staging + (uint32_t)((nstore & 1) * 4096);
+    // the store issued from this buffer two rounds ago must have read it
+    if (ring_buf == 0 && lane == 0) ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+    if (stage_and_store<OUT>(v, tmC, stg, lane, x, y, skip_store)) ++nstore;
 }
 
 __device__ __forceinline__ void fadd_bits(uint32_t& acc, uint32_t add) {

@@ -29,6 +29,8 @@ using namespace tcgemm;
 constexpr int kMaxDevices = 64;
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_100-class parts
 constexpr long long kDefaultWaitLimit = 2000000000LL;  // ~1 s at 2 GHz
+constexpr int kMinHelperSteps = 8;  // helper stream-K: fewest K steps of a tile a helper pair runs
+constexpr int kMaxHelperTiles = 8;  // helper stream-K: most tiles one helper pair runs
 
 std::mutex g_mu;
 gemm_config g_cfg = {};
@@ -293,11 +295,20 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, b
         // s = pairs / R (2..4, at least 8 K steps a part), run by s * R pairs at
         // once.  Equal parts keep the pairs that hold part j of different tiles
         // on the same K range at the same time, so tiles sharing a row block of
-        // A or a column block of B still share it in L2.  The full waves stay
-        // data-parallel.  stream_k 2 (testing) shares every tile's iterations
-        // evenly over all pairs instead.
+        // A or a column block of B still share it in L2.  When all tiles fit one
+        // wave of pairs that is more than half full (no two parts fit; long K),
+        // the R tiles run their first sk_split steps on R pairs in step with one
+        // another while the idle pairs, as helpers, run the remaining steps of
+        // up to m tiles each, one tile after another and in step with one
+        // another too.  Each tile then meets one helper's partial.  Helpers run
+        // a little slower per step (operands less shared in L2, a pipeline
+        // refill per tile, the partial to park), so they get 10 % less than an
+        // even split: steps - sk_split = 0.9 steps / (m + 1).  The full waves
+        // of larger problems stay data-parallel.
+        // stream_k 2 (testing) shares every tile's iterations evenly over all
+        // pairs instead.
         p->dp_tiles = p->num_tiles;
-        int sk_tiles = 0, sk_pairs = 0, clusters = pairs;
+        int sk_tiles = 0, sk_pairs = 0, clusters = pairs, sk_split = 0, sk_helper = 0;
         if (cfg.stream_k == 2) {
             clusters = max_pairs < kMaxSkCtas / 2 ? max_pairs : kMaxSkCtas / 2;
             sk_tiles = p->num_tiles;
@@ -313,15 +324,31 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, b
                     sk_tiles = R;
                     sk_pairs = parts * R;
                     clusters = p->num_tiles < max_pairs ? sk_pairs : pairs;
+                } else if (parts < 2 && p->num_tiles < max_pairs && 2 * R <= kMaxSkCtas) {
+                    const int KB = p->k_steps;
+                    const int m = ceil_div(R, max_pairs - R);
+                    const int l = (int)(0.9 * KB / (m + 1));
+                    // worth it only with at least kMinHelperSteps steps a helper unit,
+                    // few units a helper, and the wave at least 5 % shorter
+                    if (l >= kMinHelperSteps && m <= kMaxHelperTiles && (long long)(KB - l) * 100 <= (long long)KB * 95) {
+                        sk_tiles = R;
+                        sk_split = KB - l;
+                        sk_helper = m;
+                        sk_pairs = R + ceil_div(R, m);
+                        clusters = sk_pairs;
+                    }
                 }
             }
         }
         if (sk_tiles > 0) {
-            p->workspace_bytes = (long long)workspace_for(2 * sk_pairs);
+            // partial slots: one per sharing pair, or one per tile under helpers
+            p->workspace_bytes = (long long)workspace_for(2 * (sk_split > 0 ? sk_tiles : sk_pairs));
             if (with_workspace) {
                 p->dp_tiles = p->num_tiles - sk_tiles;
                 p->sk_tiles = sk_tiles;
                 p->sk_pairs = sk_pairs;
+                p->sk_split = sk_split;
+                p->sk_helper_tiles = sk_helper;
                 pairs = clusters;
             }
         }
@@ -673,6 +700,8 @@ int launch_planned(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int
     kp.dp_tiles = plan.dp_tiles;
     kp.sk_tiles = plan.sk_tiles;
     kp.sk_pairs = plan.sk_pairs;
+    kp.sk_split = plan.sk_split;
+    kp.sk_helper_tiles = plan.sk_helper_tiles;
     kp.c_in = accumulate ? C : nullptr;
 #ifdef TCGEMM_TRACE
     kp.trace = next_trace_slot(&kp.trace_ctas, &kp.trace_events);
@@ -838,7 +867,7 @@ int gemm_f16_device_status(int* site, int reset) {
     return v == 0 ? GEMM_OK : GEMM_ERR_DEVICE_TIMEOUT;
 }
 
-int gemm_f16_abi_version(void) { return 1; }
+int gemm_f16_abi_version(void) { return 2; }
 
 }  // extern "C"
 
@@ -886,7 +915,11 @@ unsigned check_layout(const gemm_plan& p, int acc_cols, int out_cols) {
             }
     }
     if (p.sk_tiles > 0) {
-        const long long ctas = (long long)p.sk_pairs * (kPair ? 2 : 1);
+        // partial slots: one per sharing cluster, or one per shared tile under helpers
+        const long long ctas = (long long)(p.sk_split > 0 ? p.sk_tiles : p.sk_pairs) * (kPair ? 2 : 1);
+        if (p.sk_split > 0 && (!kPair || p.sk_split >= p.k_steps || p.sk_helper_tiles < 1 ||
+                               (long long)(p.sk_pairs - p.sk_tiles) * p.sk_helper_tiles < p.sk_tiles))
+            return kSiteWorkspaceBounds;  // helpers that leave a shared tile without its rest
         if (ctas > kMaxSkCtas || (size_t)p.workspace_bytes < workspace_for((int)ctas)) return kSiteWorkspaceBounds;
         // a partial of up to 128 x (accumulator columns x lanes folded) fp32 per CTA
         if ((long long)kBM * acc_cols > kPartialFloats) return kSiteWorkspaceBounds;

@@ -383,8 +383,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; in_bounds && split > 2 && c < kChunks; ++c)
                 in_bounds = TC_CHECK(holds(sA, ring_a + ring_b, park_at(c, q), kWarpChunkBytes), kSiteSmemBounds);
             if (in_bounds && split == 1 && p.sk_tiles > 0)
-                in_bounds = TC_CHECK(cl < p.sk_pairs && cl < kMaxSkCtas, kSiteWorkspaceBounds);
+                in_bounds = TC_CHECK(sk_park_slot(p, cl, t) < sk_slots(p) && sk_slots(p) <= kMaxSkCtas,
+                                     kSiteWorkspaceBounds);
             if (!in_bounds) break;
+            // a CTA's last unit without split-K: once its accumulator is complete,
+            // every MMA and load of this CTA is done and the ring is idle (split-K
+            // keeps partials there), so a drain of more chunks than the two
+            // staging buffers hold stages every chunk in a ring buffer of its own
+            // and issues the stores back to back
+            constexpr int kChunksPerWarp = BN / kCols;
+            bool ring_drain = false;
+            if (kChunksPerWarp > 2 && split == 1 && has_k) {
+                UnitIter peek = u;
+                int t2, a2, b2;
+                ring_drain = !unit_next(peek, p, t2, a2, b2) && 4u * kChunksPerWarp * 4096u <= ring_a + ring_b &&
+                             TC_CHECK(holds(sA, ring_a + ring_b, sA + (uint32_t)(q * kChunksPerWarp * 4096),
+                                            kChunksPerWarp * 4096u),
+                                      kSiteSmemBounds);
+            }
             // Dry pass first (see dry_ok): everything the code below does once
             // the accumulator is ready, on the other accumulator, with no store,
             // no push and no hand-back; the real pass then finds the code in the
@@ -481,7 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // stream-K contributor: park this CTA's partial in its workspace
                     // slot as [column / 4][row] 16-byte groups (consecutive lanes,
                     // consecutive 16 bytes), then release this warp's flag
-                    float* slot = p.ws + (size_t)cl * kPartialFloats;
+                    const int park = sk_park_slot(p, cl, t);
+                    float* slot = p.ws + (size_t)park * kPartialFloats;
 #pragma unroll 1
                     for (int c = 0; c < BN / 32; ++c) {
                         uint32_t v[32];
@@ -498,19 +515,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __threadfence();
                     __syncwarp();
                     if (lane == 0) {
-                        ptx::st_release_gpu(p.flags + cl * 4 + q, p.epoch);
+                        ptx::st_release_gpu(p.flags + park * 4 + q, p.epoch);
                         tr(kTrParked, t);
                     }
                     continue;
                 }
-                // stream-K owner: the CTAs after this one whose shares start inside
-                // this tile hold the rest of its K range
-                int q_end = cl + 1;
+                // stream-K owner: the workspace slots [s_first, s_end) (the CTAs after
+                // this one whose shares start inside this tile) hold the rest of its K range
+                int s_first = 0, s_end = 0;
                 if (split == 1 && k1 < p.k_blocks) {
-                    const long long tile_end = (long long)(t - p.dp_tiles + 1) * p.k_blocks;
-                    while (q_end < p.sk_pairs && sk_begin(p, q_end) < tile_end) ++q_end;
-                    bool ok = true;
-                    for (int qq = cl + 1; ok && qq < q_end; ++qq) {
+                    sk_owner_slots(p, cl, t, s_first, s_end);
+                    bool ok = TC_CHECK(s_end <= sk_slots(p), kSiteWorkspaceBounds);
+                    for (int qq = s_first; ok && qq < s_end; ++qq) {
                         const unsigned* f = p.flags + qq * 4 + q;
                         int r = 1;
                         if (lane == 0) r = wait_flag(f, p.epoch, abort_flag, 4 * p.wait_limit);
@@ -525,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // launch with the same epoch (a replayed CUDA graph) waits afresh
                     __syncwarp();
                     if (lane == 0) {
-                        for (int qq = cl + 1; qq < q_end; ++qq) ptx::st_relaxed_gpu(p.flags + qq * 4 + q, 0u);
+                        for (int qq = s_first; qq < s_end; ++qq) ptx::st_relaxed_gpu(p.flags + qq * 4 + q, 0u);
                         tr(kTrFlags, t);
                     }
                 }
@@ -589,8 +605,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                         }
                     }
-                    // stream-K owner: add the contributors' partials, in CTA order
-                    for (int qq = cl + 1; qq < q_end; ++qq) {
+                    // stream-K owner: add the contributors' partials, in slot (CTA) order
+                    for (int qq = s_first; qq < s_end; ++qq) {
                         const float* slot = p.ws + (size_t)qq * kPartialFloats;
                         uint32_t x[kCols];
 #pragma unroll
@@ -602,7 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     add_c_in<OUT>(v, p, dry ? p.M : row0 + lane, nb * BN + c * kCols);  // row M: nothing read
                     store_chunk<OUT>(v, &tmC, staging, nstore, lane, nb * BN + c * kCols, dry ? p.M : row0,
-                                     dry && p.M > (1 << 30));
+                                     dry && p.M > (1 << 30),
+                                     ring_drain && !dry ? sA + (uint32_t)((q * kChunksPerWarp + c) * 4096) : 0u);
                     if (!dry && lane == 0) tr(kTrStored, c);
                     if (dry) {
                         // one chunk runs all of the loop's code; the staging is free

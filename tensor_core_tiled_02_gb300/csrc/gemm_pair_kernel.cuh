@@ -330,23 +330,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = tl & 1;
             const uint32_t aph = (tl >> 1) & 1;
             ++tl;
+            // stream-K owner (a unit that starts a tile without finishing it): the
+            // workspace slots [s_first, s_end) hold the rest of the tile's K range
+            int s_first = 0, s_end = 0;
+            if (k0 == 0 && k1 < KB) sk_owner_slots(p, cluster, t, s_first, s_end);
             // bounds-check build: everything this unit's drain touches (this warp's
-            // staging, both accumulators' columns, the workspace slot and flags)
+            // staging, both accumulators' columns, the workspace slots and flags)
             if (!(TC_CHECK(holds(sC, staging_all, staging, 2 * L::kStagingBytes), kSiteSmemBounds) &&
                   TC_CHECK(2u * L::kAccCols <= (uint32_t)L::kTmemCols, kSiteTmemBounds) &&
-                  TC_CHECK(!(k0 > 0 || k1 < KB) || (cluster < p.sk_pairs && 2 * p.sk_pairs <= kMaxSkCtas),
+                  TC_CHECK(!(k0 > 0 || k1 < KB) ||
+                               (2 * sk_slots(p) <= kMaxSkCtas && s_end <= sk_slots(p) &&
+                                (k0 == 0 || sk_park_slot(p, cluster, t) < sk_slots(p))),
                            kSiteWorkspaceBounds)))
                 break;
             const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
-            // stream-K owner: the clusters after this one whose units start inside
-            // this tile hold the rest of its K range
-            int q_end = cluster + 1;
+            // the cluster's last unit: once its accumulator is complete, every MMA
+            // and load of this CTA is done and the operand ring is idle, so a drain
+            // of more chunks than the two staging buffers hold stages every chunk
+            // in a ring buffer of its own and issues the stores back to back
+            constexpr int kChunksPerWarp = L::kAccCols / kCols;
+            bool last_unit = false, ring_drain = false;
+            if (kChunksPerWarp > 2 || (k0 == 0 && k1 < KB)) {
+                UnitIter peek = u;
+                int t2, a2, b2;
+                last_unit = !unit_next(peek, p, t2, a2, b2);
+                ring_drain = kChunksPerWarp > 2 && last_unit && KB > 0 && k0 == 0 &&
+                             4u * kChunksPerWarp * 4096u <= ring_a + ring_b &&
+                             TC_CHECK(holds(sA, ring_a + ring_b, sA + (uint32_t)(q * kChunksPerWarp * 4096),
+                                            kChunksPerWarp * 4096u),
+                                      kSiteSmemBounds);
+            }
             bool prefetched = false;
             if (k0 == 0 && k1 < KB) {
-                const long long tile_end = (long long)(t - p.dp_tiles + 1) * KB;
-                while (q_end < p.sk_pairs && sk_begin(p, q_end) < tile_end) ++q_end;
                 bool ok = true;
-                for (int qq = cluster + 1; ok && qq < q_end; ++qq) {
+                for (int qq = s_first; ok && qq < s_end; ++qq) {
                     const unsigned* f = p.flags + (qq * 2 + (int)rank) * 4 + q;
                     int r = 1;
                     if (lane == 0) r = wait_flag(f, p.epoch, abort_flag, 4 * p.wait_limit);
@@ -358,19 +375,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // launch with the same epoch (a replayed CUDA graph) waits afresh
                 __syncwarp();
                 if (lane == 0) {
-                    for (int qq = cluster + 1; qq < q_end; ++qq) ptx::st_relaxed_gpu(p.flags + (qq * 2 + (int)rank) * 4 + q, 0u);
+                    for (int qq = s_first; qq < s_end; ++qq) ptx::st_relaxed_gpu(p.flags + (qq * 2 + (int)rank) * 4 + q, 0u);
                     tr(kTrFlags, t);
                 }
                 // the owner unit is its cluster's last, so the other accumulator is
                 // free: sum the contributors' partials into it while the MMAs run
-                UnitIter peek = u;
-                int t2, a2, b2;
-                if (q_end > cluster + 1 && !unit_next(peek, p, t2, a2, b2)) {
+                if (s_end > s_first && last_unit) {
                     const uint32_t spare = lane_base + (uint32_t)((acc ^ 1) * L::kAccCols);
 #pragma unroll 1
                     for (int c = 0; c < L::kAccCols / 32; ++c) {
                         uint32_t x[32];
-                        for (int qq = cluster + 1; qq < q_end; ++qq) {
+                        for (int qq = s_first; qq < s_end; ++qq) {
                             const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
                             uint32_t y[32];
 #pragma unroll
@@ -379,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                      y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
-                                if (qq == cluster + 1)
+                                if (qq == s_first)
                                     x[i] = y[i];
                                 else
                                     fadd_bits(x[i], y[i]);
@@ -440,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < kCols; ++i) v[i] = 0u;  // empty sum (K = 0)
                     }
-                    // stream-K owner: add the contributors' partials (summed in cluster
+                    // stream-K owner: add the contributors' partials (summed in slot
                     // order), from the spare accumulator or straight from the workspace
                     if (prefetched) {
                         uint32_t x[kCols];
@@ -451,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < kCols; ++i) fadd_bits(v[i], x[i]);
                     }
-                    for (int qq = cluster + 1; !prefetched && qq < q_end; ++qq) {
+                    for (int qq = s_first; !prefetched && qq < s_end; ++qq) {
                         const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
                         uint32_t x[kCols];
 #pragma unroll
@@ -463,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     add_c_in<OUT>(v, p, dry ? p.M : row0 + lane, col0 + c * kCols);  // row M: nothing read
                     store_chunk<OUT>(v, &tmC, staging, nstore, lane, col0 + c * kCols, dry ? p.M : row0,
-                                     dry && p.M > (1 << 30));
+                                     dry && p.M > (1 << 30),
+                                     ring_drain && !dry ? sA + (uint32_t)((q * kChunksPerWarp + c) * 4096) : 0u);
                     if (!dry && lane == 0) tr(kTrStored, c);
                     if (dry) {
                         // one chunk runs all of the loop's code; the staging is free again
@@ -477,10 +493,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (failed) break;
             if (k0 > 0) {
                 const uint32_t trow = lane_base + (uint32_t)(acc * L::kAccCols);
-                // stream-K contributor: park this CTA's partial in the cluster's
-                // workspace slot as [TMEM column / 4][TMEM lane] 16-byte groups
-                // (consecutive lanes, consecutive 16 bytes), then release the flag
-                float* slot = p.ws + (size_t)(cluster * 2 + (int)rank) * kPartialFloats;
+                // stream-K contributor: park this CTA's partial in its workspace slot
+                // (the cluster's, or the tile's under helpers) as [TMEM column / 4]
+                // [TMEM lane] 16-byte groups (consecutive lanes, consecutive 16 bytes),
+                // then release the flag
+                const int park = sk_park_slot(p, cluster, t);
+                float* slot = p.ws + (size_t)(park * 2 + (int)rank) * kPartialFloats;
 #pragma unroll 1
                 for (int c = 0; c < L::kAccCols / 32; ++c) {
                     uint32_t v[32];
@@ -497,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::st_release_gpu(p.flags + (cluster * 2 + (int)rank) * 4 + q, p.epoch);
+                    ptx::st_release_gpu(p.flags + (park * 2 + (int)rank) * 4 + q, p.epoch);
                     tr(kTrParked, t);
                 }
                 continue;

@@ -45,7 +45,7 @@ def test_exports_every_declared_symbol(lib):
     assert set(names) == set(tc.EXPORTED)
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.gemm_f16_abi_version() == 1
+    assert lib.gemm_f16_abi_version() == 2
     # the product does not carry the debug variants' entry points
     for v, h in VARIANT_HEADERS.items():
         for n in declared_functions([h]):
@@ -64,7 +64,7 @@ def test_debug_variants_export_the_product_abi_and_their_own(variant):
                                     else [])
     for n in names:
         assert hasattr(vlib, n), (variant, n)
-    assert vlib.gemm_f16_abi_version() == 1
+    assert vlib.gemm_f16_abi_version() == 2
 
 
 def test_add_argument_errors_before_any_cuda_call(lib):

@@ -411,10 +411,12 @@ def test_workload_full_size_sampled(name):
     print(name, diag)
 
 
-@pytest.mark.parametrize("name", ["gemm_4096", "gemm_8192"])
+@pytest.mark.parametrize("name", ["gemm_4096", "gemm_8192", "long_k"])
 def test_workload_full_size_stream_k(name):
     """The full-size workloads through gemm_f16_ws, as the bench times them:
-    the thin last wave of tiles shared by all pairs through the workspace."""
+    the last wave of tiles shared through the workspace (a thin wave in equal
+    K parts over all pairs; long K's more than half full wave with helper
+    pairs)."""
     w = WORKLOADS[name]
     assert tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, with_workspace=True)["sk_tiles"] > 0
     a, b = workload_inputs(w)
@@ -570,3 +572,26 @@ def test_graph_replay_of_stream_k_waits_for_each_replays_partials():
         want = tc.matmul(a_d, b_d, workspace=ws)
         torch.cuda.synchronize()
         assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"replay with seed {seed}"
+
+
+
+# ---- helper stream-K: a last wave more than half full ----------------------------
+
+
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_helper_stream_k_whole(out_dtype):
+    """64 ragged pair tiles (2000 x 1800, K = 16000: 125 steps, the last one
+    ragged) on the GPU's pairs: each tile's first sk_split steps run on its own
+    pair, the idle pairs run the rest of several tiles each, and each tile
+    meets one helper's partial.  Checked whole against the oracle, and bit for
+    bit against itself on a second call (the flags are handed back)."""
+    M, N, K = 2000, 1800, 16000
+    plan = tc.gemm_f16_plan(M, N, K, out_dtype, with_workspace=True)
+    assert plan["sk_split"] > 0 and plan["sk_tiles"] == 64, plan
+    ws = tc.workspace(M, N, K, out_dtype)
+    a, b = make_inputs(M, N, K, ("normal", 1.0), ("normal", 1.0), seed_a=91, seed_b=92)
+    c = ws_gemm(a, b, out_dtype, ws)
+    parity.check(values(c), oracle_rows(a, b, out_dtype), K, out_dtype, f"helper stream-K out {out_dtype}")
+    c2 = ws_gemm(a, b, out_dtype, ws)
+    bits = torch.int16 if out_dtype == 0 else torch.int32
+    assert torch.equal(c.view(bits), c2.view(bits))

@@ -25,7 +25,18 @@ def units_of(plan, c, clusters):
         dp.append((t, 0, KB))
         t += clusters
     sk = []
-    if plan["sk_tiles"] and c < plan["sk_pairs"]:
+    if plan["sk_tiles"] and c < plan["sk_pairs"] and plan["sk_split"] > 0:
+        # helpers: pair c < sk_tiles runs steps [0, sk_split) of shared tile c; pair
+        # sk_tiles + h runs steps [sk_split, KB) of shared tiles h, h + H, ...
+        dpt, S, m = plan["dp_tiles"], plan["sk_split"], plan["sk_helper_tiles"]
+        H = plan["sk_pairs"] - plan["sk_tiles"]
+        if c < plan["sk_tiles"]:
+            sk = [(dpt + c, 0, S)]
+        else:
+            h = c - plan["sk_tiles"]
+            sk = [(dpt + t, S, KB) for t in range(h, plan["sk_tiles"], H)]
+            assert len(sk) <= m
+    elif plan["sk_tiles"] and c < plan["sk_pairs"]:
         S = plan["sk_tiles"] * KB
         it, end = S * c // plan["sk_pairs"], S * (c + 1) // plan["sk_pairs"]
         while it < end:
@@ -61,6 +72,15 @@ def check_plan(plan):
         oc, oi, on, _, ok1 = owners[0]
         n_sk = sum(1 for tt, _, _ in units_of(plan, oc, clusters) if tt >= plan["dp_tiles"])
         assert oi == n_sk - 1, "an owner unit must be its cluster's last stream-K unit"
+        if plan["sk_split"] > 0:
+            # helpers: the tile's one contributor is the helper of its index, which
+            # owns nothing, and parks in the tile's own slot
+            contributors = [u for u in units if u[3] > 0]
+            assert len(contributors) == 1 and len(units) == 2
+            hc = contributors[0][0]
+            assert hc == plan["sk_tiles"] + (t - plan["dp_tiles"]) % (plan["sk_pairs"] - plan["sk_tiles"])
+            assert all(k0 > 0 for tt, k0, _ in units_of(plan, hc, clusters) if tt >= plan["dp_tiles"])
+            continue
         # the kernel's rule for the contributors of this tile
         tile_end = (t - plan["dp_tiles"] + 1) * KB
         q_end = oc + 1
@@ -75,6 +95,7 @@ def check_plan(plan):
 
 
 SHAPES = [(8192, 8192, 8192, 0), (4096, 4096, 4096, 0), (2048, 2048, 32768, 1), (6000, 5000, 3000, 0),
+          (3072, 3072, 8192, 0), (6144, 6144, 4096, 0), (2000, 2056, 20000, 1),
           (4096, 256, 65536, 0), (20480, 20480, 1024, 0), (600, 520, 776, 0)]
 
 
@@ -84,7 +105,8 @@ SHAPES_ONE_ROW = [(128, 8192, 8192, 0), (128, 32768, 8192, 0), (100, 5000, 3000,
 
 def check_workspace(plan):
     if plan["sk_tiles"]:
-        ctas = plan["sk_pairs"] * plan["cta_group"]
+        # partial slots: one per sharing cluster, or one per shared tile under helpers
+        ctas = (plan["sk_tiles"] if plan["sk_split"] else plan["sk_pairs"]) * plan["cta_group"]
         # a fixed 16 KiB flag area (one word per epilogue warp of up to 1024 CTAs), then the partials
         assert plan["workspace_bytes"] == 1024 * 4 * 4 + ctas * 128 * 256 * 4
 
@@ -141,3 +163,30 @@ def test_one_cta_stream_k_is_opt_in():
         assert tc.gemm_f16_plan(128, 8192, 8192, 0, num_sms=152, with_workspace=True)["sk_tiles"] == 0
     finally:
         tc.gemm_f16_set_config()
+
+
+@pytest.mark.parametrize("M,N,K,dt,helpers", [(2048, 2048, 32768, 1, 11), (2000, 1800, 16000, 1, 11),
+                                              (2048, 1792, 16384, 0, 19)])
+def test_helpers_take_a_single_wave_more_than_half_full(M, N, K, dt, helpers):
+    """R tiles on P pairs with P / 2 < R < P and no other wave: the tiles run
+    their first sk_split steps on R pairs, the idle pairs run the rest, up to
+    m tiles each, with 10 % slack; the wave is at least 5 % shorter."""
+    p = tc.gemm_f16_plan(M, N, K, dt, num_sms=152, with_workspace=True)
+    R, KB, S, m = p["sk_tiles"], p["k_steps"], p["sk_split"], p["sk_helper_tiles"]
+    P = 76
+    assert p["cta_group"] == 2 and R == p["num_tiles"] and P // 2 < R < P and p["dp_tiles"] == 0
+    assert m == -(-R // (P - R)) and KB - S == int(0.9 * KB / (m + 1)) >= 8
+    assert p["sk_pairs"] - R == helpers == -(-R // m) and p["sk_pairs"] <= P
+    assert S * 100 <= KB * 95 and m * (KB - S) <= S
+    assert p["workspace_bytes"] == 16384 + 2 * R * 128 * 256 * 4
+    check_plan(p)
+    # without a workspace the wave runs whole
+    q = tc.gemm_f16_plan(M, N, K, dt, num_sms=152, with_workspace=False)
+    assert q["sk_tiles"] == 0 and q["sk_split"] == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(3072, 3072, 8192), (6144, 6144, 4096)])
+def test_no_helpers_after_full_waves(M, N, K):
+    """A last wave more than half full after full waves stays data-parallel."""
+    p = tc.gemm_f16_plan(M, N, K, 0, num_sms=152, with_workspace=True)
+    assert p["num_tiles"] > 76 and p["sk_tiles"] == 0 and p["sk_split"] == 0
