@@ -51,7 +51,7 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s (fp16 in, fp32 acc) at 8192³; % of GB300 dense FP16 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["tensor_core_tiled_02_gb300/csrc/add_kernel.cuh",
+KERNEL_SOURCES = ["tensor_core_tiled_02_gb300/csrc/add_kernel.cuh", "tensor_core_tiled_02_gb300/csrc/bounds.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_common.cuh", "tensor_core_tiled_02_gb300/csrc/gemm_kernel.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_pair_kernel.cuh", "tensor_core_tiled_02_gb300/csrc/ptx.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_f16.cu"]
