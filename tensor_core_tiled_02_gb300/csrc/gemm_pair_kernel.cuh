@@ -347,10 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the cluster's last unit: once its accumulator is complete, every MMA
             // and load of this CTA is done and the operand ring is idle, so a drain
             // of more chunks than the two staging buffers hold stages every chunk
-            // in a ring buffer of its own and issues the stores back to back
+            // in a ring buffer of its own and issues the stores back to back; and
+            // no MMA waits for the accumulator any more, so it is not handed back
             constexpr int kChunksPerWarp = L::kAccCols / kCols;
             bool last_unit = false, ring_drain = false;
-            if (kChunksPerWarp > 2 || (k0 == 0 && k1 < KB)) {
+            {
                 UnitIter peek = u;
                 int t2, a2, b2;
                 last_unit = !unit_next(peek, p, t2, a2, b2);
@@ -447,9 +448,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tmem_ld_wait();
                         if (c == L::kAccCols / kCols - 1) {
                             // this CTA's half of the accumulator is read: tell the leader
+                            // (a release at cluster scope, ~1,000 cycles: not after the
+                            // cluster's last unit, which no MMA waits for)
                             ptx::tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(dry ? dry_bar : tempty_bar(acc), 0));
+                            if (lane == 0 && (dry || !last_unit))
+                                ptx::mbar_arrive_cluster(ptx::mapa(dry ? dry_bar : tempty_bar(acc), 0));
                         }
                     } else {
 #pragma unroll
@@ -509,14 +513,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::st_global_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), v[4 * j],
                                           v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
+                // the flag first (an owner may be waiting on it), then the accumulator
+                // back to the leader, unless this is the cluster's last unit
                 ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) {
                     ptx::st_release_gpu(p.flags + (park * 2 + (int)rank) * 4 + q, p.epoch);
                     tr(kTrParked, t);
+                    if (!last_unit) ptx::mbar_arrive_cluster(ptx::mapa(tempty_bar(acc), 0));
                 }
                 continue;
             }
@@ -530,8 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before();
     __syncthreads();
-    // neither CTA leaves while the other may still signal into it
-    ptx::cluster_sync();
+    // neither CTA leaves while the other may still signal into it.  The
+    // arrival is relaxed: the barrier only marks that each CTA is done; what
+    // crosses between the CTAs went through mbarriers, and the leader's MMAs,
+    // which write the peer's Tensor Memory, completed (drain_bar) before its
+    // arrival, so the peer frees its columns only after them.
+    ptx::cluster_arrive_relaxed();
+    ptx::cluster_wait();
     if (lane == 0) tr(kTrExit);
     if (warp == 1) {
         __syncwarp();
