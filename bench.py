@@ -23,7 +23,9 @@ Prints ONE JSON line (rank 0):
              the milliseconds per launch, TFLOP/s, GB/s, its roofline (the
              tensor peak or the HBM copy rate, whichever binds) and its plan;
              then gemm_8192_sustained: the headline workload back to back for
-             a few seconds, at the power cap, with its clocks
+             a few seconds, at the power cap, with its clocks.  Beside each,
+             `cublas`: torch.mm (cuBLAS, fp16 out) on the same operands, timed
+             the same way, for comparison only
 
 ``--impl reference`` times the CPU oracle instead (the reference arm): each
 step computes a bounded sample of rows of the same product on the host cores.
@@ -72,6 +74,7 @@ def parse_args(argv=None):
     ap.add_argument("--configs", default="all",
                     help="per-config leg after the headline: 'all', 'none' or a comma list of workloads")
     ap.add_argument("--config-ms", type=float, default=30.0, help="timed milliseconds per config (at least 20 launches)")
+    ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparison in the config leg")
     ap.add_argument("--sustained-s", type=float, default=3.0,
                     help="seconds of back-to-back 8192^3 launches at the power cap (0 skips)")
     return ap.parse_args(argv)
@@ -384,7 +387,39 @@ def kernel_name(w, plan) -> str:
     return f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>"
 
 
-def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dict:
+def time_cublas(A, B, copies: int, n: int, reps: int, dev, out_dtype: int) -> float:
+    """Seconds per launch of cuBLAS's fp16 GEMM (torch.mm, fp16 output) on the
+    same rotated operands, n launches captured in a CUDA graph and replayed
+    `reps` times after a 0.2 s idle spell, as our graph leg is timed.  For
+    comparison only: our arm never calls it."""
+    import torch
+
+    C = torch.empty((copies, A.shape[1], B.shape[2]), dtype=torch.float16, device=dev)
+    cur = torch.cuda.current_stream(dev)
+    for i in range(3):
+        torch.mm(A[i % copies], B[i % copies], out=C[i % copies])
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(cur)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for i in range(n):
+            torch.mm(A[i % copies], B[i % copies], out=C[i % copies])
+    cur.wait_stream(side)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    time.sleep(0.2)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(reps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize(dev)
+    del g, C
+    return e0.elapsed_time(e1) / 1e3 / (n * reps)
+
+
+def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int, compare: bool = True) -> dict:
     """Time the GEMM of one workload on the device.  Inputs and outputs are
     rotated over enough copies that each launch reads operands evicted from
     L2.  Two timings, each with CUDA events on the launching stream around at
@@ -454,6 +489,7 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dic
     # the kernel's duration: the graph replay when it is shorter (it carries
     # no host launch cost), else the eager launches
     launch_s = min(graph_s / (n * reps), eager_s / n)
+    cublas_s = time_cublas(A, B, copies, n, reps, dev, w.out_dtype) if compare else None
     roof = gemm_roofline(w, launch_s)
     roof["traffic"] = recorded_traffic(w.name, plan)
     roof["kernel"] = kernel_name(w, plan)
@@ -466,6 +502,10 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dic
              "l2": f"rotated over {copies} copies of A, B and C, {w.bytes_moved / 1e6:.1f} MB each, "
                    f"{copies * w.bytes_moved / 1e6:.0f} MB in all (> 2x L2)",
              "plan": {k: plan[k] for k in PLAN_KEYS}}
+    if cublas_s is not None:
+        entry["cublas"] = {"ms_per_launch": cublas_s * 1e3, "ours_over_cublas_speed": cublas_s / launch_s,
+                           "what": "torch.mm, fp16 out, same operands, timed as the graph leg"
+                                   + (" (ours writes fp32)" if w.out_dtype == 1 else "")}
     if roof["frac"] < 0.2:
         entry["regime"] = ("launch latency: the roofline time is a small part of the launch, which is "
                            "fixed prologue, pipeline fill and drain")
@@ -473,7 +513,8 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int) -> dic
     return entry
 
 
-def time_sustained(w, dev, a_cpu, b_cpu, seconds: float, l2_bytes: int, sample_clocks: bool) -> dict:
+def time_sustained(w, dev, a_cpu, b_cpu, seconds: float, l2_bytes: int, sample_clocks: bool,
+                   compare: bool = True) -> dict:
     """The headline workload back to back for `seconds` (eager launches,
     inputs rotated past L2), long enough for the GPU to settle at its power
     cap; clocks sampled during the run.  Its fraction is against both the
@@ -526,9 +567,25 @@ def time_sustained(w, dev, a_cpu, b_cpu, seconds: float, l2_bytes: int, sample_c
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     tflops = w.flops / launch_s / 1e12
-    return {"workload": w.name, "seconds": launch_s * n, "launches": n, "ms_per_launch": launch_s * 1e3,
-            "tflops": tflops, "frac_of_burst": tflops / burst, "frac_of_sustained": tflops / sus,
-            "peak_source": f"bf16_tflops and bf16_tflops_sustained of {src}", "clocks": summary}
+    out = {"workload": w.name, "seconds": launch_s * n, "launches": n, "ms_per_launch": launch_s * 1e3,
+           "tflops": tflops, "frac_of_burst": tflops / burst, "frac_of_sustained": tflops / sus,
+           "peak_source": f"bf16_tflops and bf16_tflops_sustained of {src}", "clocks": summary}
+    if compare:
+        # cuBLAS's fp16 GEMM the same way, after the GPU has cooled for a second
+        time.sleep(1.0)
+        clocks = ClockSampler(dev.index or 0, enabled=sample_clocks)
+        clocks.start()
+        e0.record(cur)
+        for i in range(n):
+            j = i % copies
+            torch.mm(As[j], Bs[j], out=Cs[j])  # the sustained workload writes fp16
+        e1.record(cur)
+        torch.cuda.synchronize(dev)
+        cb_s = e0.elapsed_time(e1) / 1e3 / n
+        out["cublas"] = {"ms_per_launch": cb_s * 1e3, "tflops": w.flops / cb_s / 1e12,
+                         "ours_over_cublas_speed": cb_s / launch_s, "clocks": clocks.stop(),
+                         "what": "torch.mm, fp16 out, same operands, back to back for as long"}
+    return out
 
 
 def run_configs(args, dev, l2_bytes: int, cached_inputs: dict) -> dict:
@@ -544,7 +601,7 @@ def run_configs(args, dev, l2_bytes: int, cached_inputs: dict) -> dict:
     for name in names:
         w = WORKLOADS[name]
         a_cpu, b_cpu = cached_inputs.get(name) or workload_inputs(w)
-        out[name] = time_one_config(w, dev, a_cpu, b_cpu, args.config_ms / 1e3, l2_bytes)
+        out[name] = time_one_config(w, dev, a_cpu, b_cpu, args.config_ms / 1e3, l2_bytes, not args.no_cublas)
         torch.cuda.empty_cache()
     summary = clocks.stop()
     if summary is not None:
@@ -554,7 +611,7 @@ def run_configs(args, dev, l2_bytes: int, cached_inputs: dict) -> dict:
         a_cpu, b_cpu = cached_inputs.get(w.name) or workload_inputs(w)
         time.sleep(0.5)
         out["gemm_8192_sustained"] = time_sustained(w, dev, a_cpu, b_cpu, args.sustained_s, l2_bytes,
-                                                    not args.no_clocks)
+                                                    not args.no_clocks, not args.no_cublas)
         torch.cuda.empty_cache()
     return out
 
