@@ -68,6 +68,9 @@ struct KernelParams {
     // trace_ctas CTAs x kTraceRoles roles x trace_events records of two words
     unsigned long long* trace;
     int trace_ctas, trace_events;
+    // small launches (the pair kernel's PF instances): K steps of its first unit
+    // each CTA prefetches into L2 before the dependency wait
+    int pf_steps;
 };
 
 // ---- the trace build ------------------------------------------------------------

@@ -31,6 +31,7 @@ constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per block on
 constexpr long long kDefaultWaitLimit = 2000000000LL;  // ~1 s at 2 GHz
 constexpr int kMinHelperSteps = 8;  // helper stream-K: fewest K steps of a tile a helper pair runs
 constexpr int kMaxHelperTiles = 8;  // helper stream-K: most tiles one helper pair runs
+constexpr int kPrefetchSteps = 8;   // small pair launches: K steps each CTA prefetches into L2
 
 std::mutex g_mu;
 gemm_config g_cfg = {};
@@ -46,9 +47,9 @@ struct DeviceInfo {
     // [s]: clusters of s one-CTA-per-SM CTAs of the one-CTA kernel the GPU holds at once (0: not yet asked)
     std::atomic<int> max_clusters[kMaxSplit + 1];
     // [tile_n 64 / 128 / 256, 256 x 256 CTA pair with step K 64 / 128, blocked add,
-    // 128 x 128 CTA pair][out_dtype]: the kernel's shared-memory limit has been
-    // raised on this device
-    std::atomic<bool> attr_set[7][2];
+    // 128 x 128 CTA pair, its prefetching instance][out_dtype]: the kernel's
+    // shared-memory limit has been raised on this device
+    std::atomic<bool> attr_set[8][2];
 };
 DeviceInfo g_dev[kMaxDevices];  // static storage: every atomic starts zero
 std::mutex g_dev_mu;
@@ -497,11 +498,11 @@ int device_info(DeviceInfo** out) {
     return GEMM_OK;
 }
 
-template <int OUT, int SK, int PM = kPairBM, int PN = kPairBN>
+template <int OUT, int SK, int PM = kPairBM, int PN = kPairBN, bool PF = false>
 int launch_pair(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
-    auto kern = gemm_f16_pair_kernel<OUT, SK, PM, PN>;
-    const int rc = ensure_smem_limit(kern, kSmemLimit, dev.attr_set[PM == 128 ? 6 : SK == 128 ? 4 : 3][OUT]);
+    auto kern = gemm_f16_pair_kernel<OUT, SK, PM, PN, PF>;
+    const int rc = ensure_smem_limit(kern, kSmemLimit, dev.attr_set[PF ? 7 : PM == 128 ? 6 : SK == 128 ? 4 : 3][OUT]);
     if (rc != GEMM_OK) return rc;
     cudaLaunchConfig_t lc = {};
     lc.gridDim = dim3(plan.grid, 1, 1);
@@ -703,6 +704,12 @@ int launch_planned(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int
     kp.sk_split = plan.sk_split;
     kp.sk_helper_tiles = plan.sk_helper_tiles;
     kp.c_in = accumulate ? C : nullptr;
+    // a small pair launch (one unit per pair, at most half the SMs) starts while
+    // the previous kernel runs: its CTAs prefetch their operands into L2 first
+    // (256^3: 3.56 -> 3.34 us, 512^3: 4.51 -> 4.32 us in CUDA graphs)
+    const bool prefetch = plan.cta_group == 2 && plan.tile_m == 128 && plan.sk_tiles == 0 && plan.k_steps > 0 &&
+                          plan.num_tiles <= plan.grid / 2 && 2 * plan.grid <= dev->sms;
+    if (prefetch) kp.pf_steps = plan.k_steps < kPrefetchSteps ? plan.k_steps : kPrefetchSteps;
 #ifdef TCGEMM_TRACE
     kp.trace = next_trace_slot(&kp.trace_ctas, &kp.trace_events);
 #endif
@@ -716,6 +723,9 @@ int launch_planned(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int
     }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (prefetch)
+        return out_dtype == GEMM_OUT_F16 ? launch_pair<0, 128, 128, 128, true>(plan, ta, tb, tc, kp, s, *dev)
+                                         : launch_pair<1, 128, 128, 128, true>(plan, ta, tb, tc, kp, s, *dev);
     if (plan.cta_group == 2 && plan.tile_m == 128)
         return out_dtype == GEMM_OUT_F16 ? launch_pair<0, 128, 128, 128>(plan, ta, tb, tc, kp, s, *dev)
                                          : launch_pair<1, 128, 128, 128>(plan, ta, tb, tc, kp, s, *dev);

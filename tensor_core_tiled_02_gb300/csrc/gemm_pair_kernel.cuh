@@ -81,7 +81,14 @@ struct PairLayout {
     static constexpr int smem_bytes(int slots) { return slots * kStageBytes + kFixedBytes + 1024; }
 };
 
-template <int OUT, int SK, int PM = kPairBM, int PN = kPairBN>
+// PF: the instance for small launches (one unit per pair, at most half the SMs),
+// whose CTAs mostly start while the previous kernel in the stream still runs:
+// each producer prefetches its own unit's first pf_steps K steps into L2
+// before the dependency wait, so its loads after the wait hit L2.  (L2 is
+// where the previous kernel's writes land, so a prefetched line is never
+// stale.)  A separate instance: the extra code measurably slows the launches
+// of the other instances even when it does not run.
+template <int OUT, int SK, int PM = kPairBM, int PN = kPairBN, bool PF = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_f16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const __grid_constant__ CUtensorMap tmC, const KernelParams p) {
@@ -173,6 +180,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             UnitIter u;
             unit_iter_init(u, p, cluster, clusters);
             int t, k0, k1;
+            if constexpr (PF) {
+                UnitIter u2 = u;
+                if (unit_next(u2, p, t, k0, k1)) {
+                    int mb, nb;
+                    tile_coords(t, p, mb, nb);
+                    const int m0 = mb * PM + (int)rank * L::kRows;
+                    const int n0 = nb * PN + (int)rank * (PN / 2);
+                    const int kend = min(k1, k0 + p.pf_steps);
+                    for (int kb = k0; kb < kend; ++kb) {
+#pragma unroll
+                        for (int h = 0; h < SK / 64; ++h) ptx::tma_prefetch_2d(&tmA, kb * SK + h * 64, m0);
+#pragma unroll
+                        for (int j = 0; j < L::kBBoxes; ++j) ptx::tma_prefetch_2d(&tmB, n0 + j * 64, kb * SK);
+                    }
+                }
+            }
             while (ok && unit_next(u, p, t, k0, k1)) {
                 int mb, nb;
                 tile_coords(t, p, mb, nb);

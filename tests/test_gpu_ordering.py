@@ -43,6 +43,9 @@ CHAINS = {
     "split_k_twice": (128, 8192, 8192, 2048),    # skinny split-K, then a split-K product of its output
     "small_pair_tiles": (640, 520, 1032, 776),   # ragged 128 x 128 tiles on CTA pairs, twice
     "one_cta_then_pair": (1280, 256, 1024, 512),  # 80 one-CTA tiles, then 40 small pair tiles
+    # 12 then 6 small pair tiles: both launches prefetch their operands into L2
+    # before their dependency wait, the second while the first still writes them
+    "prefetching_pairs": (384, 256, 512, 256),
 }
 
 
