@@ -706,7 +706,7 @@ int launch_planned(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int
     kp.c_in = accumulate ? C : nullptr;
     // a small pair launch (one unit per pair, at most half the SMs) starts while
     // the previous kernel runs: its CTAs prefetch their operands into L2 first
-    // (256^3: 3.56 -> 3.34 us, 512^3: 4.51 -> 4.32 us in CUDA graphs)
+    // (256^3: 3.55 -> 3.27 us, 512^3: 4.56 -> 4.30 us in CUDA graphs)
     const bool prefetch = plan.cta_group == 2 && plan.tile_m == 128 && plan.sk_tiles == 0 && plan.k_steps > 0 &&
                           plan.num_tiles <= plan.grid / 2 && 2 * plan.grid <= dev->sms;
     if (prefetch) kp.pf_steps = plan.k_steps < kPrefetchSteps ? plan.k_steps : kPrefetchSteps;
