@@ -372,7 +372,8 @@ def gemm_roofline(w, launch_s: float) -> dict:
 
 CONFIG_WORKLOADS = ["gemm_256", "gemm_4096", "gemm_8192", "skinny", "long_k"]
 PLAN_KEYS = ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "release", "slots", "split", "grid",
-             "raster_group", "num_tiles", "k_steps", "dp_tiles", "sk_tiles", "sk_pairs", "workspace_bytes")
+             "raster_group", "num_tiles", "k_steps", "dp_tiles", "sk_tiles", "sk_pairs", "sk_split", "sk_helper_tiles",
+             "workspace_bytes")
 
 
 def rotation_copies(set_bytes: int, l2_bytes: int) -> int:
@@ -625,9 +626,7 @@ def workload_config(w, plan, copies: int | None = None) -> dict:
         cfg["l2"] = (f"inputs rotated over {copies} copies of A, B and C, {per / 1e6:.0f} MB each"
                      + (" (> L2)" if per > 126e6 else " (each set fits in L2: time includes no flush)"))
     if plan is not None:
-        cfg["plan"] = {k: plan[k] for k in ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "release", "slots", "split", "grid",
-                                            "raster_group", "num_tiles", "k_steps", "dp_tiles", "sk_tiles", "sk_pairs",
-                                            "workspace_bytes")}
+        cfg["plan"] = {k: plan[k] for k in PLAN_KEYS}
     return cfg
 
 
