@@ -22,8 +22,9 @@ Prints ONE JSON line (rank 0):
              back to back, eager and replayed from a CUDA graph; per config
              the milliseconds per launch, TFLOP/s, GB/s, its roofline (the
              tensor peak or the HBM copy rate, whichever binds) and its plan;
-             then gemm_8192_sustained: the headline workload back to back for
-             a few seconds, at the power cap, with its clocks.  Beside each,
+             then <workload>_sustained for 8192^3, long K and 4096^3: each
+             back to back for a few seconds, at the power cap, with its
+             clocks.  Beside each,
              `cublas`: torch.mm (cuBLAS, fp16 out) on the same operands, timed
              the same way, for comparison only
 
@@ -76,7 +77,9 @@ def parse_args(argv=None):
     ap.add_argument("--config-ms", type=float, default=30.0, help="timed milliseconds per config (at least 20 launches)")
     ap.add_argument("--no-cublas", action="store_true", help="skip the cuBLAS comparison in the config leg")
     ap.add_argument("--sustained-s", type=float, default=3.0,
-                    help="seconds of back-to-back 8192^3 launches at the power cap (0 skips)")
+                    help="seconds of back-to-back launches at the power cap per sustained workload (0 skips)")
+    ap.add_argument("--sustained", default="gemm_8192,long_k,gemm_4096",
+                    help="comma list of workloads timed at the power cap")
     return ap.parse_args(argv)
 
 
@@ -516,10 +519,10 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int, compar
 
 def time_sustained(w, dev, a_cpu, b_cpu, seconds: float, l2_bytes: int, sample_clocks: bool,
                    compare: bool = True) -> dict:
-    """The headline workload back to back for `seconds` (eager launches,
-    inputs rotated past L2), long enough for the GPU to settle at its power
-    cap; clocks sampled during the run.  Its fraction is against both the
-    burst and the sustained measured peak."""
+    """A workload back to back for `seconds` (eager launches, inputs rotated
+    past L2), long enough for the GPU to settle at its power cap; clocks
+    sampled during the run.  Its fraction is against both the burst and the
+    sustained measured peak."""
     import torch
 
     import tensor_core_tiled_02_gb300 as tc
@@ -573,19 +576,22 @@ def time_sustained(w, dev, a_cpu, b_cpu, seconds: float, l2_bytes: int, sample_c
            "peak_source": f"bf16_tflops and bf16_tflops_sustained of {src}", "clocks": summary}
     if compare:
         # cuBLAS's fp16 GEMM the same way, after the GPU has cooled for a second
+        Cb = Cs if w.out_dtype == 0 else [torch.empty((w.M, w.N), dtype=torch.float16, device=dev)
+                                          for _ in range(copies)]
         time.sleep(1.0)
         clocks = ClockSampler(dev.index or 0, enabled=sample_clocks)
         clocks.start()
         e0.record(cur)
         for i in range(n):
             j = i % copies
-            torch.mm(As[j], Bs[j], out=Cs[j])  # the sustained workload writes fp16
+            torch.mm(As[j], Bs[j], out=Cb[j])
         e1.record(cur)
         torch.cuda.synchronize(dev)
         cb_s = e0.elapsed_time(e1) / 1e3 / n
         out["cublas"] = {"ms_per_launch": cb_s * 1e3, "tflops": w.flops / cb_s / 1e12,
                          "ours_over_cublas_speed": cb_s / launch_s, "clocks": clocks.stop(),
-                         "what": "torch.mm, fp16 out, same operands, back to back for as long"}
+                         "what": "torch.mm, fp16 out, same operands, back to back for as long"
+                                 + (" (ours writes fp32)" if w.out_dtype == 1 else "")}
     return out
 
 
@@ -607,12 +613,12 @@ def run_configs(args, dev, l2_bytes: int, cached_inputs: dict) -> dict:
     summary = clocks.stop()
     if summary is not None:
         out["clocks"] = summary
-    if args.sustained_s > 0:
-        w = WORKLOADS["gemm_8192"]
+    for name in ([n for n in args.sustained.split(",") if n] if args.sustained_s > 0 else []):
+        w = WORKLOADS[name]
         a_cpu, b_cpu = cached_inputs.get(w.name) or workload_inputs(w)
         time.sleep(0.5)
-        out["gemm_8192_sustained"] = time_sustained(w, dev, a_cpu, b_cpu, args.sustained_s, l2_bytes,
-                                                    not args.no_clocks, not args.no_cublas)
+        out[f"{name}_sustained"] = time_sustained(w, dev, a_cpu, b_cpu, args.sustained_s, l2_bytes,
+                                                  not args.no_clocks, not args.no_cublas)
         torch.cuda.empty_cache()
     return out
 
