@@ -74,6 +74,7 @@ struct PairLayout {
     static constexpr int kOutCols = OUT == 0 ? 64 : 32;
     static constexpr int kStagingBytes = 32 * 128;
     static constexpr int kAccCols = PM == 256 ? PN : PN / 2;  // TMEM columns of one accumulator
+    static_assert(kAccCols % 64 == 0, "partials move two 32-column chunks at a time");
     static constexpr int kTmemCols = 2 * kAccCols;            // two accumulators (256 x 256: all 512)
     // full[8], empty[8], tmem_full[2], tmem_empty[2], drain, dry
     static constexpr int kNumBars = 2 * kMaxStages + 6;
@@ -406,25 +407,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // free: sum the contributors' partials into it while the MMAs run
                 if (s_end > s_first && last_unit) {
                     const uint32_t spare = lane_base + (uint32_t)((acc ^ 1) * L::kAccCols);
+                    // two 32-column chunks a round trip: the loads are latency-bound
 #pragma unroll 1
-                    for (int c = 0; c < L::kAccCols / 32; ++c) {
-                        uint32_t x[32];
+                    for (int c = 0; c < L::kAccCols / 32; c += 2) {
+                        uint32_t x0[32], x1[32];
                         for (int qq = s_first; qq < s_end; ++qq) {
                             const float* slot = p.ws + (size_t)(qq * 2 + (int)rank) * kPartialFloats;
-                            uint32_t y[32];
+                            uint32_t y0[32], y1[32];
 #pragma unroll
                             for (int j = 0; j < 8; ++j)
-                                ptx::ld_global_cg_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), y[4 * j],
-                                                     y[4 * j + 1], y[4 * j + 2], y[4 * j + 3]);
+                                ptx::ld_global_cg_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), y0[4 * j],
+                                                     y0[4 * j + 1], y0[4 * j + 2], y0[4 * j + 3]);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                ptx::ld_global_cg_v4(slot + (size_t)((((c + 1) * 8 + j) * kBM + row_in_tile) * 4),
+                                                     y1[4 * j], y1[4 * j + 1], y1[4 * j + 2], y1[4 * j + 3]);
 #pragma unroll
                             for (int i = 0; i < 32; ++i) {
-                                if (qq == s_first)
-                                    x[i] = y[i];
-                                else
-                                    fadd_bits(x[i], y[i]);
+                                if (qq == s_first) {
+                                    x0[i] = y0[i];
+                                    x1[i] = y1[i];
+                                } else {
+                                    fadd_bits(x0[i], y0[i]);
+                                    fadd_bits(x1[i], y1[i]);
+                                }
                             }
                         }
-                        ptx::tmem_st_32x32b_x32(spare + (uint32_t)(c * 32), x);
+                        ptx::tmem_st_32x32b_x32(spare + (uint32_t)(c * 32), x0);
+                        ptx::tmem_st_32x32b_x32(spare + (uint32_t)((c + 1) * 32), x1);
                     }
                     ptx::tmem_st_wait();
                     prefetched = true;
@@ -526,15 +536,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // then release the flag
                 const int park = sk_park_slot(p, cluster, t);
                 float* slot = p.ws + (size_t)(park * 2 + (int)rank) * kPartialFloats;
+                // two 32-column chunks a TMEM round trip
 #pragma unroll 1
-                for (int c = 0; c < L::kAccCols / 32; ++c) {
-                    uint32_t v[32];
-                    ptx::tmem_ld_32x32b_x32(trow + c * 32, v);
+                for (int c = 0; c < L::kAccCols / 32; c += 2) {
+                    uint32_t v0[32], v1[32];
+                    ptx::tmem_ld_32x32b_x32(trow + c * 32, v0);
+                    ptx::tmem_ld_32x32b_x32(trow + (c + 1) * 32, v1);
                     ptx::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
-                        ptx::st_global_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), v[4 * j],
-                                          v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        ptx::st_global_v4(slot + (size_t)(((c * 8 + j) * kBM + row_in_tile) * 4), v0[4 * j],
+                                          v0[4 * j + 1], v0[4 * j + 2], v0[4 * j + 3]);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        ptx::st_global_v4(slot + (size_t)((((c + 1) * 8 + j) * kBM + row_in_tile) * 4), v1[4 * j],
+                                          v1[4 * j + 1], v1[4 * j + 2], v1[4 * j + 3]);
                 }
                 // the flag first (an owner may be waiting on it), then the accumulator
                 // back to the leader, unless this is the cluster's last unit
