@@ -385,9 +385,14 @@ def rotation_copies(set_bytes: int, l2_bytes: int) -> int:
     return max(3, math.ceil(2 * l2_bytes / max(set_bytes, 1)))
 
 
-def kernel_name(w, plan) -> str:
+def kernel_name(w, plan, sms: int = 152) -> str:
+    """The kernel instance the plan launches (the library's dispatch rule)."""
     if plan["cta_group"] == 2:
-        return f"gemm_f16_pair_kernel<{w.out_dtype},{plan['tile_k']},{plan['tile_m']},{plan['tile_n']}>"
+        # small pair launches (128 x 128 tiles filling at most half the pairs, no
+        # shared tile) take the instance that prefetches its operands into L2
+        pf = int(plan["tile_m"] == 128 and plan["sk_tiles"] == 0 and plan["k_steps"] > 0
+                 and plan["num_tiles"] <= plan["grid"] // 2 and 2 * plan["grid"] <= sms)
+        return f"gemm_f16_pair_kernel<{w.out_dtype},{plan['tile_k']},{plan['tile_m']},{plan['tile_n']},{pf}>"
     return f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>"
 
 
@@ -496,7 +501,7 @@ def time_one_config(w, dev, a_cpu, b_cpu, target_s: float, l2_bytes: int, compar
     cublas_s = time_cublas(A, B, copies, n, reps, dev, w.out_dtype) if compare else None
     roof = gemm_roofline(w, launch_s)
     roof["traffic"] = recorded_traffic(w.name, plan)
-    roof["kernel"] = kernel_name(w, plan)
+    roof["kernel"] = kernel_name(w, plan, torch.cuda.get_device_properties(dev).multi_processor_count)
     entry = {"M": w.M, "N": w.N, "K": w.K, "out_dtype": "f16" if w.out_dtype == 0 else "f32",
              "ms_per_launch": launch_s * 1e3, "eager_ms_per_launch": eager_s / n * 1e3,
              "graph_ms_per_launch": graph_s / (n * reps) * 1e3,
@@ -718,7 +723,7 @@ def run_ours(args, w, dist: Dist):
     if dist.rank == 0:
         roofline = gemm_roofline(w, avg_launch_s)
         roofline["traffic"] = recorded_traffic(w.name, plan)
-        roofline["kernel"] = kernel_name(w, plan)
+        roofline["kernel"] = kernel_name(w, plan, torch.cuda.get_device_properties(dev).multi_processor_count)
         roofline["avg_launch_ms"] = avg_launch_s * 1e3
         cpu = None
         if not args.no_cpu_baseline and dist.world == 1:
