@@ -296,16 +296,18 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, b
         // s = pairs / R (2..4, at least 8 K steps a part), run by s * R pairs at
         // once.  Equal parts keep the pairs that hold part j of different tiles
         // on the same K range at the same time, so tiles sharing a row block of
-        // A or a column block of B still share it in L2.  When all tiles fit one
-        // wave of pairs that is more than half full (no two parts fit; long K),
-        // the R tiles run their first sk_split steps on R pairs in step with one
-        // another while the idle pairs, as helpers, run the remaining steps of
-        // up to m tiles each, one tile after another and in step with one
-        // another too.  Each tile then meets one helper's partial.  Helpers run
-        // a little slower per step (operands less shared in L2, a pipeline
-        // refill per tile, the partial to park), so they get 10 % less than an
-        // even split: steps - sk_split = 0.9 steps / (m + 1).  The full waves
-        // of larger problems stay data-parallel.
+        // A or a column block of B still share it in L2.  When the last wave is
+        // more than half full (no two parts fit), the R tiles run their first
+        // sk_split steps on R pairs in step with one another while the pairs
+        // idle in that wave, as helpers, run the remaining steps of up to m
+        // tiles each, one tile after another and in step with one another too.
+        // Each tile then meets one helper's partial.  Helpers run a little
+        // slower per step (operands less shared in L2, a pipeline refill per
+        // tile, the partial to park), so they get 10 % less than an even split:
+        // steps - sk_split = 0.9 steps / (m + 1).  Shared units run first; the
+        // full waves, data-parallel, follow (1024 x 8192 x 8192: 85.7 -> 82.7
+        // us).  Even shares of the last wave over all pairs instead start the
+        // pairs at scattered K offsets, lose the L2 sharing and gain nothing.
         // stream_k 2 (testing) shares every tile's iterations evenly over all
         // pairs instead.
         p->dp_tiles = p->num_tiles;
@@ -325,7 +327,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, b
                     sk_tiles = R;
                     sk_pairs = parts * R;
                     clusters = p->num_tiles < max_pairs ? sk_pairs : pairs;
-                } else if (parts < 2 && p->num_tiles < max_pairs && 2 * R <= kMaxSkCtas) {
+                } else if (parts < 2 && 2 * R <= kMaxSkCtas) {
                     const int KB = p->k_steps;
                     const int m = ceil_div(R, max_pairs - R);
                     const int l = (int)(0.9 * KB / (m + 1));
@@ -336,7 +338,7 @@ int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, b
                         sk_split = KB - l;
                         sk_helper = m;
                         sk_pairs = R + ceil_div(R, m);
-                        clusters = sk_pairs;
+                        clusters = p->num_tiles < max_pairs ? sk_pairs : pairs;
                     }
                 }
             }

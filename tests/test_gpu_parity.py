@@ -595,3 +595,21 @@ def test_helper_stream_k_whole(out_dtype):
     c2 = ws_gemm(a, b, out_dtype, ws)
     bits = torch.int16 if out_dtype == 0 else torch.int32
     assert torch.equal(c.view(bits), c2.view(bits))
+
+
+@pytest.mark.parametrize("M,N,K,out_dtype", [(1000, 7992, 8200, 0), (1000, 7424, 3456, 1)])
+def test_helper_stream_k_after_full_waves_whole(M, N, K, out_dtype):
+    """A full wave of pair tiles, then a last wave more than half full whose
+    tiles take helpers (shared units first, the data-parallel wave after them
+    on every pair); ragged M, N and K.  Checked whole against the oracle, and
+    bit for bit against itself on a second call."""
+    plan = tc.gemm_f16_plan(M, N, K, out_dtype, with_workspace=True)
+    pairs = plan["grid"] // 2
+    assert plan["dp_tiles"] >= pairs and plan["sk_split"] > 0 and plan["sk_pairs"] < pairs, plan
+    ws = tc.workspace(M, N, K, out_dtype)
+    a, b = make_inputs(M, N, K, ("normal", 1.0), ("normal", 1.0), seed_a=97, seed_b=98)
+    c = ws_gemm(a, b, out_dtype, ws)
+    parity.check(values(c), oracle_rows(a, b, out_dtype), K, out_dtype, f"helpers after full waves, out {out_dtype}")
+    c2 = ws_gemm(a, b, out_dtype, ws)
+    bits = torch.int16 if out_dtype == 0 else torch.int32
+    assert torch.equal(c.view(bits), c2.view(bits))

@@ -185,8 +185,25 @@ def test_helpers_take_a_single_wave_more_than_half_full(M, N, K, dt, helpers):
     assert q["sk_tiles"] == 0 and q["sk_split"] == 0
 
 
-@pytest.mark.parametrize("M,N,K", [(3072, 3072, 8192), (6144, 6144, 4096)])
-def test_no_helpers_after_full_waves(M, N, K):
-    """A last wave more than half full after full waves stays data-parallel."""
+@pytest.mark.parametrize("M,N,K,helpers", [(6144, 6144, 4096, True), (1024, 8192, 8192, True),
+                                           (3072, 3072, 8192, False), (2048, 4096, 4096, False)])
+def test_helpers_after_full_waves(M, N, K, helpers):
+    """After full waves, a last wave more than half full takes helpers by the
+    same rule (at most 8 tiles a helper, at least 8 steps a helper unit, the
+    wave at least 5 % shorter); the full waves run data-parallel after the
+    shared units, on every pair.  3072 x 3072 would need 9 tiles a helper,
+    2048 x 4096 x 4096 helper units of 5 steps: both stay data-parallel."""
     p = tc.gemm_f16_plan(M, N, K, 0, num_sms=152, with_workspace=True)
-    assert p["num_tiles"] > 76 and p["sk_tiles"] == 0 and p["sk_split"] == 0
+    P, KB, T = 76, p["k_steps"], p["num_tiles"]
+    R = T % P
+    assert p["cta_group"] == 2 and T > P and P // 2 < R
+    if not helpers:
+        assert p["sk_tiles"] == 0 and p["dp_tiles"] == T
+        return
+    m = -(-R // (P - R))
+    assert (p["sk_tiles"], p["dp_tiles"], p["sk_helper_tiles"]) == (R, T - R, m)
+    assert KB - p["sk_split"] == int(0.9 * KB / (m + 1)) >= 8 and m <= 8
+    assert p["sk_pairs"] == R + -(-R // m) <= P and p["grid"] == 2 * P
+    assert p["workspace_bytes"] == 16384 + 2 * R * 128 * 256 * 4
+    check_plan(p)
+    check_workspace(p)

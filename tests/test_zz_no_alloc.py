@@ -84,11 +84,12 @@ def bits(c):
 CASES = [((4096, 4096, 4096, 0), {}),
          ((1100, 1280, 2056, 1), dict(cta_group=2, stream_k=2)),
          ((128, 8192, 8192, 0), dict(cta_group=1, stream_k=2)),
-         ((2000, 1800, 16000, 1), {})]
+         ((2000, 1800, 16000, 1), {}),
+         ((1000, 7424, 3456, 1), {})]
 
 
 @pytest.mark.parametrize("shape,cfg", CASES, ids=["4096_tail_stream_k", "every_tile_shared", "one_row_every_sm",
-                                                  "helper_pairs"])
+                                                  "helper_pairs", "helpers_after_a_full_wave"])
 def test_noalloc_matches_workspace_entry_on_two_calls(shape, cfg):
     lib = tc.load_library()
     M, N, K, out_dtype = shape
