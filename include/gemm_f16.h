@@ -90,8 +90,9 @@ typedef struct {
     long long workspace_bytes;  /* workspace gemm_f16_ws needs for its stream-K plan; 0 if none */
     int sk_split;               /* 0: the shared K iterations are dealt out in even contiguous shares;
                                    > 0 (CTA pairs, a last wave more than half full): pair i runs K steps
-                                   [0, sk_split) of shared tile i, and the idle pairs ("helpers") run
-                                   steps [sk_split, k_steps) of the shared tiles, one after another */
+                                   [0, sk_split) of shared tile dp_tiles + i, and the pairs idle in that
+                                   wave ("helpers") run steps [sk_split, k_steps) of the shared tiles, one
+                                   after another; the data-parallel tiles follow on every pair */
     int sk_helper_tiles;        /* with sk_split > 0: shared tiles each helper pair runs */
 } gemm_plan;
 
