@@ -504,6 +504,37 @@ def test_extreme_shapes_sampled(M, N, K, out_dtype):
     parity.check(values(c)[ii, jj], e, K, out_dtype, f"{M}x{N}x{K} elements")
 
 
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_output_beyond_2_31_elements_sampled(out_dtype):
+    """C of 65 536 x 32 776 (2^31 + 2^19 elements, 4.3 or 8.6 GB): the rows
+    past element 2^31 (byte offsets past 4 and 8 GiB) are written, and read
+    back by C += A.B, at the right places.  Checked on the rows around the
+    2^31-element boundary, the last rows and a few random ones, copied back
+    row by row; each row of C depends on the same row of A only, so the
+    oracle computes those rows from A's."""
+    M, N, K = 1 << 16, (1 << 15) + 8, 64
+    a, b = make_inputs(M, N, K, ("uniform", 1.0), ("uniform", 1.0), seed_a=17, seed_b=18)
+    dt = torch.float16 if out_dtype == 0 else torch.float32
+    a_d, b_d = a.cuda(), b.cuda()
+    c = tc.matmul(a_d, b_d, out_dtype=dt)
+    torch.cuda.synchronize()
+    edge = (1 << 31) // N
+    rows = np.array(sorted({0, edge - 1, edge, edge + 1, M - 2, M - 1} |
+                           set(np.random.default_rng(5).integers(0, M, 6).tolist())), np.int64)
+    idx = torch.from_numpy(rows).cuda()
+    got = c[idx].cpu()
+    a_rows = a.numpy()[rows]
+    parity.check(values(got), oracle_rows(torch.from_numpy(a_rows), b, out_dtype), K, out_dtype,
+                 f"C beyond 2^31 elements, out {out_dtype}")
+    tc.matmul_acc(a_d, b_d, c)
+    torch.cuda.synchronize()
+    got2 = c[idx].cpu()
+    del c
+    torch.cuda.empty_cache()
+    ref2 = oracle.as_values(oracle.gemm_acc(a_rows, b.numpy(), got.numpy(), out_dtype), out_dtype)
+    parity.check(values(got2), ref2, K, out_dtype, f"C += A.B beyond 2^31 elements, out {out_dtype}")
+
+
 # ---- CUDA graphs ----------------------------------------------------------------------
 
 
