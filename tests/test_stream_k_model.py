@@ -207,3 +207,27 @@ def test_helpers_after_full_waves(M, N, K, helpers):
     assert p["workspace_bytes"] == 16384 + 2 * R * 128 * 256 * 4
     check_plan(p)
     check_workspace(p)
+
+
+def test_schedules_of_random_shapes():
+    """Every stream-K schedule the planner makes for 400 seeded random shapes
+    (M, N, K up to 12 288, both output types, three SM counts, with the
+    workspace) covers each (tile, K step) once and keeps the owner and
+    contributor rules: parts, even shares, helpers alone or after full
+    waves, and one-CTA plans."""
+    import numpy as np
+
+    rng = np.random.default_rng(2024)
+    kinds = set()
+    for _ in range(400):
+        M = int(rng.integers(1, 12289))
+        N = 8 * int(rng.integers(1, 1537))
+        K = 8 * int(rng.integers(1, 1537))
+        dt = int(rng.integers(0, 2))
+        sms = int(rng.choice([152, 148, 132]))
+        p = tc.gemm_f16_plan(M, N, K, dt, num_sms=sms, with_workspace=True)
+        check_plan(p)
+        check_workspace(p)
+        if p["sk_tiles"]:
+            kinds.add(("helpers" if p["sk_split"] else "shares") + (" after waves" if p["dp_tiles"] else " alone"))
+    assert {"shares after waves", "helpers alone", "helpers after waves"} <= kinds, kinds
