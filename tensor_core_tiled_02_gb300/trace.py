@@ -10,9 +10,12 @@ back to back through that library, reads the stamps and summarises them as
 the time of each point after the end of the previous launch in the stream.
 
     python -m tensor_core_tiled_02_gb300.trace --workload skinny --launches 32 --graph
+    python -m tensor_core_tiled_02_gb300.trace --shape 1024,8192,8192 --config cta_group=2,stream_k=2
 
-builds the trace library if needed, runs the workload (inputs rotated past
-L2, as the bench does) and prints the table.  Only the trace library is used
+builds the trace library if needed, runs the workload or shape (inputs
+rotated past L2, as the bench does; a shape takes U[-1,1] operands and fp16
+output unless a fourth field says 1, fp32) under the given tuning config and
+prints the table.  Only the trace library is used
 in this process: run it on its own, not inside a process that has loaded the
 product library.
 """
@@ -268,24 +271,53 @@ def format_table(summary: dict, title: str) -> str:
     return "\n".join(lines)
 
 
+def parse_shape(text: str):
+    """'M,N,K' or 'M,N,K,out_dtype' -> (M, N, K, out_dtype)."""
+    parts = [int(x) for x in text.split(",")]
+    if len(parts) not in (3, 4) or min(parts[:3]) < 0 or (len(parts) == 4 and parts[3] not in (0, 1)):
+        raise ValueError(f"shape must be M,N,K or M,N,K,out_dtype (0 fp16, 1 fp32), got {text!r}")
+    return (*parts[:3], parts[3] if len(parts) == 4 else 0)
+
+
+def parse_config(text: str) -> dict:
+    """'key=value,...' (the fields of gemm_config) -> keyword arguments of
+    gemm_f16_set_config."""
+    cfg = {}
+    for item in filter(None, text.split(",")):
+        key, sep, value = item.partition("=")
+        if not sep:
+            raise ValueError(f"config items are key=value, got {item!r}")
+        cfg[key.strip()] = int(value)
+    return cfg
+
+
 def main(argv=None):
-    from tensor_core_tiled_02_gb300.synthetic import WORKLOADS
+    from tensor_core_tiled_02_gb300.synthetic import WORKLOADS, Workload
 
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--workload", default="skinny", choices=[n for n, w in WORKLOADS.items() if w.kind == "gemm"])
+    ap.add_argument("--shape", default="", help="M,N,K[,out_dtype] instead of a workload")
+    ap.add_argument("--config", default="", help="tuning config, e.g. cta_group=2,stream_k=2")
     ap.add_argument("--launches", type=int, default=32)
     ap.add_argument("--graph", action="store_true", help="capture the launches in a CUDA graph and replay it")
     ap.add_argument("--copies", type=int, default=0, help="input copies to rotate over (0: past L2, as the bench)")
     ap.add_argument("--json", default="", help="also write the summary here")
     ap.add_argument("--npz", default="", help="also write the raw records and the plan here")
     args = ap.parse_args(argv)
-    w = WORKLOADS[args.workload]
+    if args.shape:
+        M, N, K, dt = parse_shape(args.shape)
+        w = Workload(f"{M}x{N}x{K}", M, N, K, ("uniform", 1.0), ("uniform", 1.0), dt)
+    else:
+        w = WORKLOADS[args.workload]
+    cfg = parse_config(args.config)
     copies = args.copies or max(3, math.ceil(2 * 129 * 2 ** 20 / w.bytes_moved))
     copies = min(copies, args.launches)
-    rec, plan, _, _, _ = capture(w.M, w.N, w.K, w.out_dtype, args.launches, args.graph, copies, w.a_dist, w.b_dist)
+    rec, plan, _, _, _ = capture(w.M, w.N, w.K, w.out_dtype, args.launches, args.graph, copies, w.a_dist, w.b_dist,
+                                 config=cfg)
     problems = check_records(rec, plan)
     s = summarise(rec)
-    title = f"{w.name} {w.M}x{w.N}x{w.K}, {'graph' if args.graph else 'eager'}, {args.launches} launches"
+    title = (w.name if args.shape else f"{w.name} {w.M}x{w.N}x{w.K}") + (f" ({args.config})" if cfg else "") + \
+        f", {'graph' if args.graph else 'eager'}, {args.launches} launches"
     print(format_table(s, title))
     print(f"plan: cta_group {plan['cta_group']}, tile {plan['tile_m']}x{plan['tile_n']}x{plan['tile_k']}, "
           f"split {plan['split']}, grid {plan['grid']}, stream-K tiles {plan['sk_tiles']}")

@@ -2,6 +2,7 @@
 them (include/gemm_f16_trace.h) are decoded into GPU time, with the global
 timer wrapping modulo 2^32 between launches, and summarised."""
 import numpy as np
+import pytest
 
 from tensor_core_tiled_02_gb300 import trace as tr
 
@@ -44,3 +45,15 @@ def test_summary_is_relative_to_the_previous_launch_end():
     # the producers' loads 1 us after their entries: 1.4 and 1.5 us, median 1.45
     assert abs(s["first step's loads issued"] - 1.45) < 1e-9
     assert abs(s["last CTA exits"] - 10.0) < 1e-9
+
+
+def test_shape_and_config_arguments():
+    assert tr.parse_shape("1024,8192,8192") == (1024, 8192, 8192, 0)
+    assert tr.parse_shape("2048,2048,32768,1") == (2048, 2048, 32768, 1)
+    for bad in ("1024,8192", "1,2,3,4,5", "1,2,3,2", "-1,2,3"):
+        with pytest.raises(ValueError):
+            tr.parse_shape(bad)
+    assert tr.parse_config("") == {}
+    assert tr.parse_config("cta_group=2,stream_k=2") == {"cta_group": 2, "stream_k": 2}
+    with pytest.raises(ValueError):
+        tr.parse_config("cta_group")
