@@ -57,6 +57,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = ["tensor_core_tiled_02_gb300/csrc/add_kernel.cuh", "tensor_core_tiled_02_gb300/csrc/bounds.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_common.cuh", "tensor_core_tiled_02_gb300/csrc/gemm_kernel.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_pair_kernel.cuh", "tensor_core_tiled_02_gb300/csrc/ptx.cuh",
+                  "tensor_core_tiled_02_gb300/csrc/gemm_small_kernel.cuh",
                   "tensor_core_tiled_02_gb300/csrc/gemm_f16.cu"]
 
 
@@ -235,6 +236,8 @@ def kernel_source_hash() -> str:
 def kernel_family(plan: dict) -> str:
     if plan.get("kind") == "add":
         return "add_f32_kernel"
+    if plan.get("cta_group") == 1 and plan.get("tile_m", 128) < 128:
+        return "gemm_f16_small_kernel"
     return "gemm_f16_pair_kernel" if plan.get("cta_group") == 2 else "gemm_f16_kernel"
 
 
@@ -393,6 +396,8 @@ def kernel_name(w, plan, sms: int = 152) -> str:
         pf = int(plan["tile_m"] == 128 and plan["sk_tiles"] == 0 and plan["k_steps"] > 0
                  and plan["num_tiles"] <= plan["grid"] // 2 and 2 * plan["grid"] <= sms)
         return f"gemm_f16_pair_kernel<{w.out_dtype},{plan['tile_k']},{plan['tile_m']},{plan['tile_n']},{pf}>"
+    if plan["tile_m"] < 128:
+        return f"gemm_f16_small_kernel<{w.out_dtype},{plan['tile_m']}>"
     return f"gemm_f16_kernel<{plan['tile_n']},{w.out_dtype}>"
 
 

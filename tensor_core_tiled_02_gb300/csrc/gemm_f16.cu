@@ -21,6 +21,7 @@
 #include "add_kernel.cuh"
 #include "gemm_kernel.cuh"
 #include "gemm_pair_kernel.cuh"
+#include "gemm_small_kernel.cuh"
 
 namespace {
 
@@ -47,9 +48,10 @@ struct DeviceInfo {
     // [s]: clusters of s one-CTA-per-SM CTAs of the one-CTA kernel the GPU holds at once (0: not yet asked)
     std::atomic<int> max_clusters[kMaxSplit + 1];
     // [tile_n 64 / 128 / 256, 256 x 256 CTA pair with step K 64 / 128, blocked add,
-    // 128 x 128 CTA pair, its prefetching instance][out_dtype]: the kernel's
-    // shared-memory limit has been raised on this device
-    std::atomic<bool> attr_set[8][2];
+    // 128 x 128 CTA pair, its prefetching instance, small kernel of 8 / 16 / 32
+    // rows][out_dtype]: the kernel's shared-memory limit has been raised on this
+    // device
+    std::atomic<bool> attr_set[11][2];
 };
 DeviceInfo g_dev[kMaxDevices];  // static storage: every atomic starts zero
 std::mutex g_dev_mu;
@@ -147,6 +149,29 @@ int smem_for_pair(int out_dtype, int step_k, int pair_m, int slots) {
     return out_dtype == GEMM_OUT_F16 ? PairLayout<0, 64>::smem_bytes(slots) : PairLayout<1, 64>::smem_bytes(slots);
 }
 
+int smem_for_small(int out_dtype, int rows, int k_blocks) {
+    if (out_dtype == GEMM_OUT_F16)
+        return rows == 8 ? SmallLayout<0, 8>::smem_bytes(k_blocks)
+               : rows == 16 ? SmallLayout<0, 16>::smem_bytes(k_blocks) : SmallLayout<0, 32>::smem_bytes(k_blocks);
+    return rows == 8 ? SmallLayout<1, 8>::smem_bytes(k_blocks)
+           : rows == 16 ? SmallLayout<1, 16>::smem_bytes(k_blocks) : SmallLayout<1, 32>::smem_bytes(k_blocks);
+}
+
+// Small problems, under the default config only: the rows of C per CTA of
+// the small kernel (one CTA per rows x 64 tile, every K step loaded at once,
+// so K <= 1024): the fewest of 8, 16, 32 that keep the tiles within one
+// wave; 0 when the small kernel does not take the problem.
+int small_rows(int M, int N, int K, int num_sms, const gemm_config& cfg) {
+    if (cfg.tile_n || cfg.cta_group || cfg.split || cfg.stream_k || cfg.grid || cfg.tile_k || cfg.stages ||
+        cfg.release)
+        return 0;
+    if (M <= 0 || N <= 0 || K <= 0 || ceil_div(K, 64) > kSmallMaxKB) return 0;
+    const long long cols = ceil_div(N, kSmallBN);
+    for (int rows : {8, 16, 32})
+        if ((long long)ceil_div(M, rows) * cols <= num_sms) return rows;
+    return 0;
+}
+
 int max_slots_for(int tile_n, int out_dtype) {
     int s = kMaxStages;
     while (s > 1 && smem_for(tile_n, out_dtype, s) > kSmemLimit) --s;
@@ -207,6 +232,25 @@ Fit fit_estimate(int num_sms) {
 int plan_impl(int M, int N, int K, int out_dtype, int num_sms, const Fit& fit, bool with_workspace,
               const gemm_config& cfg, gemm_plan* p) {
     std::memset(p, 0, sizeof(*p));
+    if (const int rows = small_rows(M, N, K, num_sms, cfg)) {
+        p->cta_group = 1;
+        p->tile_m = rows;
+        p->tile_n = kSmallBN;
+        p->tile_k = 64;
+        p->tiles_m = ceil_div(M, rows);
+        p->tiles_n = ceil_div(N, kSmallBN);
+        p->num_tiles = p->tiles_m * p->tiles_n;
+        p->k_steps = ceil_div(K, 64);
+        p->stages = p->slots = p->k_steps;  // every K block in flight at once
+        p->split = 1;
+        p->grid = p->num_tiles;
+        p->raster_group = 1;
+        p->dp_tiles = p->num_tiles;
+        p->tmem_cols = 32;
+        p->smem_bytes = smem_request(smem_for_small(out_dtype, rows, p->k_steps), p->tmem_cols);
+        p->threads = kSmallThreads;
+        return GEMM_OK;
+    }
     int max_pairs = fit.clusters[2];
     p->tile_m = kBM;
     p->tile_k = kBK;
@@ -528,6 +572,30 @@ int launch_pair(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap&
     return GEMM_OK;
 }
 
+template <int OUT, int NT>
+int launch_small(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, void* C, const KernelParams& kp,
+                 cudaStream_t stream, DeviceInfo& dev) {
+    auto kern = gemm_f16_small_kernel<OUT, NT>;
+    const int rc = ensure_smem_limit(kern, kSmemLimit, dev.attr_set[NT == 8 ? 8 : NT == 16 ? 9 : 10][OUT]);
+    if (rc != GEMM_OK) return rc;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3(plan.grid, 1, 1);
+    lc.blockDim = dim3(kSmallThreads, 1, 1);
+    lc.dynamicSmemBytes = plan.smem_bytes;
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&lc, kern, ta, tb, C, kp);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
 template <int BN, int OUT>
 int launch(const gemm_plan& plan, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
            const KernelParams& kp, cudaStream_t stream, DeviceInfo& dev) {
@@ -725,6 +793,15 @@ int launch_planned(const gemm_f16_t* A, const gemm_f16_t* B, void* C, int M, int
     }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (plan.cta_group == 1 && plan.tile_m < kBM) {
+        if (out_dtype == GEMM_OUT_F16)
+            return plan.tile_m == 8 ? launch_small<0, 8>(plan, ta, tb, C, kp, s, *dev)
+                   : plan.tile_m == 16 ? launch_small<0, 16>(plan, ta, tb, C, kp, s, *dev)
+                                       : launch_small<0, 32>(plan, ta, tb, C, kp, s, *dev);
+        return plan.tile_m == 8 ? launch_small<1, 8>(plan, ta, tb, C, kp, s, *dev)
+               : plan.tile_m == 16 ? launch_small<1, 16>(plan, ta, tb, C, kp, s, *dev)
+                                   : launch_small<1, 32>(plan, ta, tb, C, kp, s, *dev);
+    }
     if (prefetch)
         return out_dtype == GEMM_OUT_F16 ? launch_pair<0, 128, 128, 128, true>(plan, ta, tb, tc, kp, s, *dev)
                                          : launch_pair<1, 128, 128, 128, true>(plan, ta, tb, tc, kp, s, *dev);
@@ -941,6 +1018,18 @@ unsigned check_layout(const gemm_plan& p, int acc_cols, int out_cols) {
 
 }  // namespace
 
+// The small kernel's carve-up (K blocks, the C tile, the barriers) inside the
+// shared memory the plan asks for, its K blocks within the kernel's limit,
+// one tile per CTA and its 32 TMEM columns.
+template <class L>
+unsigned check_small(const gemm_plan& p) {
+    if (p.k_steps < 1 || p.k_steps > kSmallMaxKB || p.grid != p.num_tiles || p.split != 1) return kSiteSmemBounds;
+    const long long need = 1023 + (long long)p.k_steps * L::kBlockBytes + L::kStageBytes + (kSmallMaxKB + 1) * 8 + 8;
+    if (need > p.smem_bytes || p.smem_bytes > kSmemLimit) return kSiteSmemBounds;
+    if (p.tmem_cols != L::kTmemCols) return kSiteTmemBounds;
+    return 0;
+}
+
 extern "C" int gemm_f16_check_plan(const gemm_plan* plan, int out_dtype, int* site) {
     if (!plan || !site) return GEMM_ERR_NULL;
     *site = 0;
@@ -961,6 +1050,12 @@ extern "C" int gemm_f16_check_plan(const gemm_plan* plan, int out_dtype, int* si
         s = f16 ? check_layout<Layout<128, 0>, false>(p, 128, 64) : check_layout<Layout<128, 1>, false>(p, 128, 32);
     else if (p.cta_group == 1 && p.tile_m == 128 && p.tile_k == 64 && p.tile_n == 64)
         s = f16 ? check_layout<Layout<64, 0>, false>(p, 64, 64) : check_layout<Layout<64, 1>, false>(p, 64, 32);
+    else if (p.cta_group == 1 && p.tile_n == kSmallBN && p.tile_k == 64 && p.tile_m == 8)
+        s = f16 ? check_small<SmallLayout<0, 8>>(p) : check_small<SmallLayout<1, 8>>(p);
+    else if (p.cta_group == 1 && p.tile_n == kSmallBN && p.tile_k == 64 && p.tile_m == 16)
+        s = f16 ? check_small<SmallLayout<0, 16>>(p) : check_small<SmallLayout<1, 16>>(p);
+    else if (p.cta_group == 1 && p.tile_n == kSmallBN && p.tile_k == 64 && p.tile_m == 32)
+        s = f16 ? check_small<SmallLayout<0, 32>>(p) : check_small<SmallLayout<1, 32>>(p);
     *site = (int)s;
     return s == 0 ? GEMM_OK : GEMM_ERR_CONFIG;
 }

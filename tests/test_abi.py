@@ -123,15 +123,16 @@ def test_empty_problems_are_noops(lib):
 def test_plan_matches_the_tiling_arithmetic(lib):
     """Sequential steps = K / tile_k for each workload; one CTA (or CTA pair)
     per output tile; tiles = ceil(M/tile_m) * ceil(N/tile_n)."""
-    # sequential steps of 64 (one CTA per tile) or 128 (CTA pairs) along K
-    want_k_steps = {"gemm_256": 2, "gemm_4096": 32, "gemm_8192": 64, "skinny": 128, "long_k": 256}
+    # sequential steps of 64 (one CTA per tile, or the small kernel's K blocks)
+    # or 128 (CTA pairs) along K
+    want_k_steps = {"gemm_256": 4, "gemm_4096": 32, "gemm_8192": 64, "skinny": 128, "long_k": 256}
     for name, w in WORKLOADS.items():
         if w.kind != "gemm":
             continue
         p = tc.gemm_f16_plan(w.M, w.N, w.K, w.out_dtype, num_sms=152)
         assert p["k_steps"] == want_k_steps[name] == w.K // p["tile_k"]
         assert p["tile_k"] == 64 * p["cta_group"]
-        assert (p["tile_m"], p["tile_n"]) in ({1: [(128, 64), (128, 128), (128, 256)],
+        assert (p["tile_m"], p["tile_n"]) in ({1: [(128, 64), (128, 128), (128, 256), (8, 64), (16, 64), (32, 64)],
                                                 2: [(256, 256), (128, 128)]}[p["cta_group"]])
         assert p["tiles_m"] == -(-w.M // p["tile_m"]) and p["tiles_n"] == -(-w.N // p["tile_n"])
         assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
@@ -144,13 +145,20 @@ def test_plan_matches_the_tiling_arithmetic(lib):
         assert 1 <= p["stages"] <= 8 and p["release"] < p["stages"]
         assert p["slots"] == p["stages"] + p["release"]
         assert p["smem_bytes"] <= 232448
-    # the 256^3 case is 2 x 2 tiles of 128 x 128, each on a CTA pair (64 rows per
-    # SM) with 2 K steps of 128; on single CTAs, the pages' tiling: 4 K steps of 64
+    # the 256^3 case goes to the small kernel: 32 x 4 tiles of 8 x 64 on 128
+    # CTAs, 4 K blocks of 64; on CTA pairs, 2 x 2 tiles of 128 x 128 (64 rows
+    # per SM) with 2 K steps of 128; on single CTAs, the pages' tiling: 4 K
+    # steps of 64
     p = tc.gemm_f16_plan(256, 256, 256, 0, num_sms=152)
     assert (p["tiles_m"], p["tiles_n"], p["tile_m"], p["tile_n"], p["k_steps"], p["cta_group"], p["grid"]) == \
-        (2, 2, 128, 128, 2, 2, 8)
-    assert p["tmem_cols"] == 128
+        (32, 4, 8, 64, 4, 1, 128)
+    assert p["tmem_cols"] == 32
     try:
+        tc.gemm_f16_set_config(cta_group=2, tile_n=128)
+        p = tc.gemm_f16_plan(256, 256, 256, 0, num_sms=152)
+        assert (p["tiles_m"], p["tiles_n"], p["tile_m"], p["tile_n"], p["k_steps"], p["cta_group"], p["grid"]) == \
+            (2, 2, 128, 128, 2, 2, 8)
+        assert p["tmem_cols"] == 128
         tc.gemm_f16_set_config(cta_group=1)
         p = tc.gemm_f16_plan(256, 256, 256, 0, num_sms=152)
         assert (p["tiles_m"], p["tiles_n"], p["tile_n"], p["k_steps"], p["cta_group"]) == (2, 2, 128, 4, 1)
@@ -296,9 +304,13 @@ def test_plan_ragged_and_degenerate(lib):
     # small problems: 128 x 128 tiles on CTA pairs with 128-deep steps
     p = tc.gemm_f16_plan(300, 392, 520, 0, num_sms=152)
     assert (p["cta_group"], p["tiles_m"], p["tiles_n"], p["k_steps"], p["grid"]) == (2, 3, 4, 5, 24)
+    # the smallest: the small kernel, one CTA of 8 x 64
     p = tc.gemm_f16_plan(1, 8, 8, 1, num_sms=152)
-    assert (p["num_tiles"], p["k_steps"], p["grid"]) == (1, 1, 2)
+    assert (p["cta_group"], p["tile_m"], p["tile_n"], p["num_tiles"], p["k_steps"], p["grid"]) == (1, 8, 64, 1, 1, 1)
     try:
+        tc.gemm_f16_set_config(cta_group=2)
+        p = tc.gemm_f16_plan(1, 8, 8, 1, num_sms=152)
+        assert (p["num_tiles"], p["k_steps"], p["grid"]) == (1, 1, 2)
         tc.gemm_f16_set_config(cta_group=1)
         p = tc.gemm_f16_plan(300, 392, 520, 0, num_sms=152)
         assert (p["tiles_m"], p["tiles_n"], p["k_steps"]) == (3, 4, 9)
@@ -315,6 +327,7 @@ def test_stages_clamp_and_release_rule(lib):
     ring holds stages + release buffers.  stages is clamped to the steps one
     CTA runs and must exceed release, as emit_pipeline requires."""
     try:
+        tc.gemm_f16_set_config(cta_group=2)
         p = tc.gemm_f16_plan(128, 128, 256, 0, num_sms=152)  # one small pair tile: 2 steps of 128
         assert (p["cta_group"], p["stages"], p["slots"]) == (2, 2, 2)
         tc.gemm_f16_set_config(cta_group=1)
@@ -380,7 +393,8 @@ def _check_plan(p, M, N, K, auto):
     assert p["num_tiles"] == p["tiles_m"] * p["tiles_n"]
     assert p["k_steps"] == cdiv(K, p["tile_k"])
     assert p["stages"] > p["release"] >= 0 and p["slots"] == p["stages"] + p["release"]
-    assert p["smem_bytes"] <= 232448 and p["threads"] == 192
+    small = p["cta_group"] == 1 and p["tile_m"] < 128
+    assert p["smem_bytes"] <= 232448 and p["threads"] == (128 if small else 192)
     # one CTA per SM at most as far as TMEM goes: no CTA ever waits on another's columns
     assert 233472 // (p["smem_bytes"] + 1024) * p["tmem_cols"] <= 512
     if p["cta_group"] == 2:
@@ -393,6 +407,14 @@ def _check_plan(p, M, N, K, auto):
             assert 0 < p["workspace_bytes"] <= (20 << 20) + 16384  # gemm_f16_noalloc's array holds it
         else:
             assert p["dp_tiles"] == p["num_tiles"]
+    elif small:
+        # the small kernel (default config only): one CTA per tile of 8, 16 or 32
+        # rows by 64 columns, one wave, K <= 512 in blocks of 64 loaded at once
+        assert auto and p["tile_m"] in (8, 16, 32) and (p["tile_n"], p["tile_k"], p["tmem_cols"]) == (64, 64, 32)
+        assert p["grid"] == p["num_tiles"] <= 152 and p["split"] == 1 and 1 <= p["k_steps"] <= 8
+        assert p["stages"] == p["slots"] == p["k_steps"] and p["sk_tiles"] == 0
+        # the fewest rows that keep the tiles within one wave
+        assert p["tile_m"] == 8 or cdiv(M, p["tile_m"] // 2) * p["tiles_n"] > 152
     else:
         assert p["tile_m"] == 128 and p["tile_n"] in (64, 128, 256) and p["tmem_cols"] == 2 * p["tile_n"]
         if p["split"] > 1:

@@ -89,9 +89,24 @@ def test_planted_mistakes_are_caught(check_lib):
     p.smem_bytes -= 2048
     assert site_of(check_lib, p, 0) == SMEM
     # more ring slots than the kernel has barriers for
-    p = plan_struct(256, 256, 256, 0)
+    p = plan_struct(256, 256, 256, 0, cta_group=2)
     p.slots = 9
     assert site_of(check_lib, p, 0) == SMEM
+    # the small kernel: shared memory short by two KiB, more K blocks than it
+    # holds, a CTA short of its tile, half its Tensor Memory
+    p = plan_struct(256, 256, 256, 0)
+    assert (p.tile_m, p.tile_n) == (8, 64)
+    p.smem_bytes -= 2048
+    assert site_of(check_lib, p, 0) == SMEM
+    p = plan_struct(256, 256, 256, 0)
+    p.k_steps = 9
+    assert site_of(check_lib, p, 0) == SMEM
+    p = plan_struct(256, 256, 256, 0)
+    p.grid -= 1
+    assert site_of(check_lib, p, 0) == SMEM
+    p = plan_struct(256, 256, 256, 0)
+    p.tmem_cols //= 2
+    assert site_of(check_lib, p, 0) == TMEM
     # half the Tensor Memory the two accumulators need
     p = plan_struct(128, 8192, 8192, 0)
     p.tmem_cols //= 2

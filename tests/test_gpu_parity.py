@@ -644,3 +644,35 @@ def test_helper_stream_k_after_full_waves_whole(M, N, K, out_dtype):
     c2 = ws_gemm(a, b, out_dtype, ws)
     bits = torch.int16 if out_dtype == 0 else torch.int32
     assert torch.equal(c.view(bits), c2.view(bits))
+
+
+# ---- the small kernel ----------------------------------------------------------------
+
+
+SMALL_SHAPES = [(256, 256, 256, 0, 8), (1, 8, 8, 1, 8), (8, 64, 64, 0, 8), (300, 264, 504, 0, 16),
+                (200, 520, 504, 1, 16), (512, 512, 512, 1, 32), (64, 4096, 512, 0, 32), (37, 1000, 72, 0, 8),
+                (129, 616, 448, 1, 16), (600, 376, 264, 0, 32)]
+
+
+@pytest.mark.parametrize("M,N,K,out_dtype,rows", SMALL_SHAPES)
+def test_small_kernel_whole(M, N, K, out_dtype, rows):
+    """Problems the small kernel takes (one CTA per rows x 64 tile of C, the
+    transposed MMA with M = 64, K <= 512 loaded at once), ragged in M, N and
+    K: C = A.B and then C += A.B checked whole against the oracle, and the
+    product bit for bit on a second call."""
+    plan = tc.gemm_f16_plan(M, N, K, out_dtype)
+    assert (plan["cta_group"], plan["tile_m"], plan["tile_n"]) == (1, rows, 64), plan
+    a, b = make_inputs(M, N, K, ("normal", 1.0), ("normal", 1.0), seed_a=M, seed_b=N + K)
+    a_d, b_d = a.cuda(), b.cuda()
+    dt = torch.float16 if out_dtype == 0 else torch.float32
+    c = tc.matmul(a_d, b_d, out_dtype=dt)
+    c2 = tc.matmul(a_d, b_d, out_dtype=dt)
+    torch.cuda.synchronize()
+    parity.check(values(c.cpu()), oracle_rows(a, b, out_dtype), K, out_dtype, f"small {M}x{N}x{K}")
+    bits = torch.int16 if out_dtype == 0 else torch.int32
+    assert torch.equal(c.view(bits), c2.view(bits))
+    c0 = c.cpu()
+    tc.matmul_acc(a_d, b_d, c)
+    torch.cuda.synchronize()
+    ref = oracle.as_values(oracle.gemm_acc(a.numpy(), b.numpy(), c0.numpy(), out_dtype), out_dtype)
+    parity.check(values(c.cpu()), ref, K, out_dtype, f"small {M}x{N}x{K}, C += A.B")

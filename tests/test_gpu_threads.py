@@ -2,9 +2,9 @@
 
 The per-device facts the library caches (SM count, cluster capacity, each
 kernel's raised shared-memory limit) are filled on first use.  A fresh
-process starts four threads that wait on one barrier and then call, each on
-its own CUDA stream, a different kernel: a CTA-pair GEMM, a split-K GEMM, a
-one-CTA GEMM and the blocked add.  Every result is checked against the
+process starts six threads that wait on one barrier and then call, each on
+its own CUDA stream, a different kernel: CTA-pair GEMMs of both tile sizes, a
+split-K GEMM, a one-CTA GEMM, the small kernel and the blocked add.  Every result is checked against the
 oracle (the add bit for bit).
 """
 import os
@@ -31,7 +31,7 @@ SCRIPT = textwrap.dedent("""
     from tensor_core_tiled_02_gb300.synthetic import make_inputs, add_inputs
 
     jobs = [("pair", 2048, 2048, 512, 0), ("split", 128, 1024, 4096, 1), ("one", 1280, 1024, 256, 0),
-            ("pair128", 384, 640, 256, 0)]
+            ("pair128", 384, 640, 768, 0), ("small", 256, 256, 256, 1)]
     inputs = {{name: make_inputs(M, N, K, ("uniform", 1.0), ("uniform", 1.0), seed_a=i, seed_b=i + 10)
               for i, (name, M, N, K, _) in enumerate(jobs)}}
     x_cpu, y_cpu = add_inputs(256, 512)
@@ -82,14 +82,15 @@ SCRIPT = textwrap.dedent("""
 
 def test_first_calls_from_several_threads():
     plan_names = {"pair": (2048, 2048, 512, 0), "split": (128, 1024, 4096, 1), "one": (1280, 1024, 256, 0),
-                  "pair128": (384, 640, 256, 0)}
+                  "pair128": (384, 640, 768, 0), "small": (256, 256, 256, 1)}
     import tensor_core_tiled_02_gb300 as tc
     plans = {k: tc.gemm_f16_plan(*v) for k, v in plan_names.items()}
-    # the four GEMMs really take four different paths
+    # the five GEMMs really take five different paths
     assert plans["pair"]["cta_group"] == 2 and plans["pair"]["tile_m"] == 256
     assert plans["split"]["cta_group"] == 1 and plans["split"]["split"] > 1
     assert plans["one"]["cta_group"] == 1 and plans["one"]["split"] == 1
     assert plans["pair128"]["cta_group"] == 2 and plans["pair128"]["tile_m"] == 128
+    assert plans["small"]["cta_group"] == 1 and plans["small"]["tile_m"] == 8
     code = SCRIPT.format(root=ROOT, tests=os.path.join(ROOT, "tests"))
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stdout[-2000:] + out.stderr[-4000:]
