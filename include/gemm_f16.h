@@ -71,7 +71,9 @@ typedef enum {
 typedef struct {
     int cta_group;              /* 1: one CTA per tile; 2: a CTA pair (two SMs) per tile,
                                    256 x 256 or 128 x 128 */
-    int tile_m, tile_n, tile_k; /* output tile and K step (elements) */
+    int tile_m, tile_n, tile_k; /* output tile and K step (elements); tile_m 8, 16 or 32 with
+                                   tile_n 64 (cta_group 1, 128 threads): the small-problem kernel,
+                                   one wave of CTAs holding all of K (at most 512) at once */
     int tiles_m, tiles_n;       /* ceil(M/tile_m), ceil(N/tile_n) */
     int num_tiles;              /* tiles_m * tiles_n: one owner CTA each */
     int k_steps;                /* ceil(K/tile_k): the sequential pipeline length */
