@@ -81,7 +81,8 @@ typedef struct {
     int release;                /* extra steps before a buffer is reused (delay_release) */
     int slots;                  /* shared-memory ring buffers: stages + release */
     int split;                  /* CTAs (one thread-block cluster) sharing each tile along K */
-    int grid;                   /* CTAs launched: persistent, or num_tiles * split with split-K */
+    int grid;                   /* CTAs launched: persistent, num_tiles * split with split-K, or
+                                   num_tiles (the small kernel) */
     int raster_group;           /* m-blocks per raster group */
     int smem_bytes;             /* dynamic shared memory per CTA */
     int tmem_cols;              /* Tensor Memory columns per CTA */
