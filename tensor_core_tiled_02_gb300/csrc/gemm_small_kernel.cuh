@@ -169,6 +169,14 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
+    if (warp == 1) {
+        // the accumulator is read (or never will be): its columns go back now,
+        // while the stores run; every MMA completed first (the done barrier,
+        // committed even after an abort)
+        if (go && lane == 0 && !have) wait_drain(done_bar, 0, p.wait_limit);
+        __syncwarp();
+        ptx::tmem_dealloc(tmem, L::kTmemCols);
+    }
     // an aborted launch (a wait gave up somewhere) stores nothing
     const bool store = have && *abort_flag == 0;
     if (store) {
@@ -214,13 +222,6 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         // after an abort the producer lets every copy it issued land before the
         // CTA (and its shared memory) goes away
         for (int kb = 0; kb < KB; ++kb) wait_drain(bar0 + 8u * kb, 0, p.wait_limit);
-    }
-    if (warp == 1) {
-        // every MMA completed (the done barrier: committed even after an abort)
-        // before the columns are freed
-        if (go && lane == 0 && !have) wait_drain(done_bar, 0, p.wait_limit);
-        __syncwarp();
-        ptx::tmem_dealloc(tmem, L::kTmemCols);
     }
     if (lane == 0) tr(kTrExit);
 }
